@@ -1,0 +1,356 @@
+"""Benchmark of the Muon optimizer step on one B300 (or N replicas under torchrun).
+
+Workload: the d26 stack -- 26 layers of width 1664, per layer four 1664 x 1664
+attention matrices, the 6656 x 1664 MLP input and the 1664 x 6656 MLP output
+(156 fp32 matrices, 8.64e8 elements) -- one Muon step per timed step: Nesterov
+momentum (beta 0.95), Frobenius normalisation, 5 quintic Newton-Schulz
+iterations, aspect-scaled update (lr 0.02).  Consecutive steps carry the
+momentum and weights and read the next of four pre-drawn gradient sets (each
+3.46 GB, far above the 126 MB L2, so no flush is needed between steps).
+
+Metric: algorithmic Newton-Schulz TFLOP/s of the whole step (3 m^2 n + m^3 per
+matrix and iteration, m <= n the oriented sides) = flops / step time; the line
+also carries ms per step, the NS kernels' own TFLOP/s and their fraction of the
+measured bf16 peak.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon optimizer step ms and NS TFLOP/s at d26 shapes; fraction of bf16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "d26"
+WORKLOAD_DESC = ("d26 stack: 156 fp32 matrices (26 layers x [4 x 1664x1664, 6656x1664, 1664x6656]), "
+                 "Nesterov beta 0.95, lr 0.02, 5 Newton-Schulz iterations, momentum carried across steps")
+
+
+def workload_desc(name):
+    if name == WORKLOAD:
+        return WORKLOAD_DESC
+    import workloads
+    shapes = workloads.config_shapes(name)
+    kinds = sorted(set(shapes))
+    return (f"{name}: {len(shapes)} fp32 matrices of shapes {kinds}, Nesterov beta 0.95, lr 0.02, "
+            "5 Newton-Schulz iterations")
+
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and clock-event reasons through NVML every 100 ms."""
+
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, index: int):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._nvml = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # no NVML: the line says so
+            self._nvml = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._nvml.nvmlDeviceGetClockInfo(self._h, self._nvml.NVML_CLOCK_SM))
+                mask = self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for name, bit in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            self._stop.wait(0.1)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if self._nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample(idx=(0, 4), workload=WORKLOAD):
+    """Time the fp64 oracle on a bounded sample of the workload: one full Muon
+    step of the listed matrices (for d26: 0 is 1664 x 1664, 4 is 6656 x 1664).
+    Returns (TFLOP/s of algorithmic NS flops, seconds, description, threads, flops)."""
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+    idx = list(idx)
+    p, g, m, shapes = workloads.make_stack(workload, "cpu", indices=idx)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for pi, gi, mi, (r, c) in zip(p, g, m, shapes):
+        oracle.muon_matrix(pi.numpy(), gi.numpy(), mi.numpy(), lr=np.float32(0.02), beta=np.float32(0.95),
+                           nesterov=True, ns_steps=5)
+        mm, nn = min(r, c), max(r, c)
+        flops += 5 * (3 * mm * mm * nn + mm ** 3)
+    dt = time.perf_counter() - t0
+    desc = (f"oracle (fp64 C, OpenMP) full Muon step of {workload} matrices "
+            + ", ".join(f"{i} ({r}x{c})" for i, (r, c) in zip(idx, shapes))
+            + f"; {flops:.3e} algorithmic NS flops")
+    return flops / dt / 1e12, dt, desc, oracle.num_threads(), flops
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    # one matrix per step keeps --steps 20 --warmup 3 within a few minutes
+    for _ in range(args.warmup):
+        oracle_sample((0,), args.workload)
+    times, flops_total = [], 0.0
+    for _ in range(args.steps):
+        tf, dt, desc, cores, flops = oracle_sample((0,), args.workload)
+        times.append(dt)
+        flops_total += flops
+    value = flops_total / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(args.workload), "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import pretraining_optimizer_step_b300 as mu
+    import workloads
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_src = load_peaks()
+
+    # CPU oracle timed first (rank 0, N = 1 only), before any GPU work
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, desc, cores, _ = oracle_sample((0, 4) if args.workload == WORKLOAD else (0,), args.workload)
+        cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{desc}; {dt:.1f} s"}
+
+    wl = args.workload
+    shapes = workloads.config_shapes(wl)
+    seed = rank  # each replica works on its own stack
+    p, g0, m, _ = workloads.make_stack(wl, dev, seed=seed)
+    n_sets = 4
+    grads = [g0] + [[workloads.make_grad(wl, i, s, dev, seed, step) for i, s in enumerate(shapes)]
+                    for step in range(1, n_sets)]
+    stream = torch.cuda.Stream(device=dev)
+    step_args = [mu.StepArgs(p, grads[k], m, shapes) for k in range(n_sets)]
+    hp = workloads.HYPER
+    elems = sum(r * c for r, c in shapes)
+
+    def step(k):
+        mu.muon_step(step_args[k % n_sets], lr=hp["lr"], beta=hp["beta"], nesterov=hp["nesterov"],
+                     ns_steps=hp["ns_steps"], stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+
+    def timed(nsteps, fn):
+        barrier()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for k in range(nsteps):
+            fn(k)
+        ev1.record(stream)
+        ev1.synchronize()
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        if dist is not None:
+            t = torch.tensor([ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    # ---- timed region 1: plain steps (the headline value)
+    mu.muon_init()
+    for k in range(args.warmup):
+        step(k)
+    mu.muon_get_status(stream)
+    with ClockSampler(local_rank) as clocks:
+        total_ms = timed(args.steps, step)
+    mu.muon_get_status(stream)
+    info = mu.muon_get_step_info()
+    ms_step = total_ms / args.steps
+    flops_step = info["ns_alg_flops"]
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # ---- timed region 2: same steps with CUDA events around every launch
+    mu.muon_destroy()
+    mu.muon_init(debug_flags=mu.MUON_DEBUG_TIME_KERNELS)
+    for k in range(args.warmup):
+        step(k)
+    mu.muon_get_status(stream)
+    mu.muon_kernel_times()
+    timed_ms2 = timed(args.steps, step)
+    kt = mu.muon_kernel_times()
+    mu.muon_get_status(stream)
+    ns_kinds = ("gram", "poly", "axpy", "axpy_update")
+    ns_ms = sum(kt[k][0] for k in ns_kinds)
+    ns_launches = sum(kt[k][1] for k in ns_kinds)
+    ns_tflops = flops_step * args.steps / (ns_ms * 1e-3) / 1e12
+    mom_ms, mom_launches = kt["momentum_norm"]
+    mom_bytes = 14.0 * elems * args.steps
+    mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9
+    q = mu.muon_plan_query(shapes, hp["ns_steps"])
+    peak_tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_tf_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_bw = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("bytes_per_launch_d26")
+        except (OSError, ValueError):
+            traffic = None
+    roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (Gram, polynomial, axpy launches)",
+                "achieved": ns_tflops, "peak": peak_tf, "unit": "TFLOP/s", "frac": ns_tflops / peak_tf,
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "frac_of_sustained": ns_tflops / peak_tf_sus,
+                "traffic": traffic,
+                "avg_launch_ms": ns_ms / max(ns_launches, 1),
+                "alg_flops_per_launch": flops_step * args.steps / max(ns_launches, 1),
+                "executed_over_alg_flops": q["ns_executed_flops"] / q["ns_alg_flops"]}
+    roofline_hbm = {"bound": "hbm", "kernel": "momentum_norm_kernel", "achieved": mom_gbs, "peak": peak_bw,
+                    "unit": "GB/s", "frac": mom_gbs / peak_bw, "peak_source": f"{peak_src} hbm_gbs",
+                    "alg_bytes_per_launch": mom_bytes / max(mom_launches, 1),
+                    "avg_launch_ms": mom_ms / max(mom_launches, 1)}
+    phase_ms = {k: v[0] / args.steps for k, v in kt.items()}
+
+    # ---- end to end through the C ABI with host buffers: each step copies its
+    # gradients from pinned host memory and reads the updated weights back
+    e2e = None
+    if not args.no_e2e:
+        mu.muon_destroy()
+        mu.muon_init()
+        host_g = [[t.cpu().pin_memory() for t in grads[k]] for k in range(2)]
+        host_p = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in p]
+        dev_g = [torch.empty_like(t) for t in g0]
+        e2e_args = mu.StepArgs(p, dev_g, m, shapes)
+        h2d = sum(t.numel() * 4 for t in host_g[0])
+        d2h = sum(t.numel() * 4 for t in host_p)
+
+        def e2e_step(k):
+            with torch.cuda.stream(stream):
+                for d, h in zip(dev_g, host_g[k % 2]):
+                    d.copy_(h, non_blocking=True)
+            mu.muon_step(e2e_args, lr=hp["lr"], beta=hp["beta"], nesterov=hp["nesterov"],
+                         ns_steps=hp["ns_steps"], stream=stream)
+            with torch.cuda.stream(stream):
+                for h, d in zip(host_p, p):
+                    h.copy_(d, non_blocking=True)
+
+        e2e_steps = max(1, min(args.steps, 5))
+        e2e_step(0)
+        stream.synchronize()
+        ms_e2e = timed(e2e_steps, e2e_step) / e2e_steps
+        mu.muon_get_status(stream)
+        e2e = {"value": world * flops_step / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "path": "pinned host grads -> muon_step (C ABI) -> pinned host params, one stream"}
+    mu.muon_destroy()
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": workload_desc(wl), "matrices": len(shapes), "elements": elems,
+                           "ns_alg_flops_per_step": flops_step,
+                           "parallelism": "replicas" if world > 1 else "single-gpu",
+                           "l2": (f"no flush: 4 rotating gradient sets of {4 * elems / 1e9:.2f} GB; weights "
+                                  f"and momentum {4 * elems / 1e9:.2f} GB each"
+                                  + (", all far above the 126 MB L2" if 4 * elems > 126e6 * 4
+                                     else " (below 126 MB L2: small case)")),
+                           "state_dtype": "fp32 p/g/m; bf16 Newton-Schulz operands, fp32 accumulation"},
+                "ns_tflops": ns_tflops, "frac_of_bf16_peak": ns_tflops / peak_tf,
+                "phase_ms_per_step": phase_ms, "timed_ms_with_kernel_events": timed_ms2 / args.steps,
+                "roofline": roofline, "roofline_elementwise": roofline_hbm, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks.summary(), "gpu_launches": info["launches"] * args.steps,
+                "workspace_bytes": info["workspace_bytes"]}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="d26 (the measured workload) or a smaller case for profiling: d2, d12, d20, sweep_*")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    rc = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+/*
+ * muon.h -- C ABI of the B300 (sm_103a) Muon optimizer-step library (libmuon.so).
+ *
+ * The operation is the Muon step of the nanochat pretraining recipe as the page
+ * "Cara Melatih ChatGPT Sendiri dengan Budget 50 Dolar" (apidog.com) describes
+ * it in section "2. Pengoptimal Muon (nanochat/optim.py)" (and its dev.to
+ * translation, section "2. ตัวปรับปรุง Muon"): every 2-D weight matrix gets a
+ * momentum update, the update direction is normalised and driven toward its
+ * orthogonal polar factor by quintic Newton-Schulz iterations (one (a, b, c)
+ * row per iteration: A = X X^T, B = b A + c A A, X <- a X + B X), and the
+ * weight moves along the result.  The pages print neither the momentum form
+ * nor the normalisation nor the update scale; this library takes
+ *
+ *   m' = beta m + g                       (stored back into the momentum buffer)
+ *   u  = nesterov ? g + beta m' : m'
+ *   X0 = u / (||u||_F + eps), transposed first when rows > cols (long side = columns)
+ *   K iterations with rows 0..K-1 of the coefficient table
+ *   O  = X_K, transposed back;  p <- p - lr * sqrt(max(1, rows/cols)) * O
+ *
+ * (momentum_mode 1 uses m' = beta m + (1-beta) g, u = nesterov ? (1-beta) g + beta m' : m').
+ *
+ * Precision: p, g, m are float32 (fp32 state); the Newton-Schulz operands X, A,
+ * B are stored as bfloat16 (round to nearest even) and every product
+ * accumulates in fp32; the last iteration's result O is formed in fp32 and
+ * applied to p without being stored.
+ *
+ * Conventions shared by every entry point:
+ *  - All functions return a muon_status; none aborts, throws or prints.
+ *  - Matrices are dense, contiguous, row-major float32 arrays in device memory
+ *    of the device that was current at muon_init, owned by the caller.
+ *  - Work is enqueued on the caller's CUDA stream and is asynchronous; argument
+ *    errors are reported synchronously, device-side errors (a timed-out wait,
+ *    an out-of-range tile) are latched in a device status word and returned by
+ *    muon_get_status.
+ *  - One process-global context; the functions are not thread-safe.
+ */
+#ifndef MUON_H
+#define MUON_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Every entry point below is exported with default visibility; the library
+ * hides everything else. */
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* muon_stream_t;
+
+typedef enum muon_status {
+    MUON_OK = 0,
+    MUON_ERR_INVALID_ARG = 1,         /* NULL pointer, n_mats < 0, ns_steps out of range, bad config */
+    MUON_ERR_UNSUPPORTED_SHAPE = 2,   /* rows or cols < 8 or not a multiple of 8 (16-byte bf16 rows) */
+    MUON_ERR_MISALIGNED = 3,          /* a matrix pointer is not 16-byte aligned */
+    MUON_ERR_NOT_INITIALIZED = 4,     /* muon_init has not succeeded */
+    MUON_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed */
+    MUON_ERR_OUT_OF_MEMORY = 6,       /* workspace allocation failed */
+    MUON_ERR_DEVICE_TIMEOUT = 7,      /* a kernel's bounded wait expired (device status) */
+    MUON_ERR_DEVICE_BOUNDS = 8,       /* a kernel saw an out-of-range tile (device status) */
+    MUON_ERR_UNSUPPORTED_DEVICE = 9   /* no device, or the current device is not sm_103 */
+} muon_status;
+
+/* Stored (PyTorch (out_features, in_features)) shape of one parameter matrix. */
+typedef struct muon_shape {
+    int rows;
+    int cols;
+} muon_shape;
+
+enum {
+    MUON_MOMENTUM_SGD_NESTEROV = 0, /* m' = beta m + g (default) */
+    MUON_MOMENTUM_EMA = 1           /* m' = beta m + (1 - beta) g */
+};
+
+enum {
+    MUON_DEBUG_KEEP_O = 1,            /* also write O (fp32, stored layout) for muon_debug_copy_ns_output */
+    MUON_DEBUG_POISON_WORKSPACE = 2,  /* fill the bf16 workspace with NaN before every step */
+    MUON_DEBUG_TIME_KERNELS = 4,      /* record CUDA events around every launch (muon_kernel_times) */
+    MUON_DEBUG_INJECT_LOST_LOAD = 8   /* test hook: one operand load of the first Gram launch is never
+                                         issued, so the consumer's bounded wait must expire and the step
+                                         reports MUON_ERR_DEVICE_TIMEOUT; the result is then invalid */
+};
+
+typedef struct muon_config {
+    const double* coeffs;   /* (a, b, c) rows, one per Newton-Schulz iteration, row-major; NULL
+                               selects the default: (3.4445, -4.7750, 2.0315) for every row */
+    int n_coeff_rows;       /* rows in coeffs (1..16); ignored when coeffs is NULL (then 5) */
+    double eps;             /* added to ||u||_F before dividing; <= 0 selects 1e-7 */
+    int momentum_mode;      /* MUON_MOMENTUM_* */
+    int debug_flags;        /* MUON_DEBUG_* bit set; 0 for production */
+    double wait_timeout_s;  /* limit of every in-kernel wait; <= 0 selects 5 s */
+} muon_config;
+
+/*
+ * Create the process-global context on the current CUDA device.
+ * cfg may be NULL (all defaults).  The coefficient table is copied.
+ * Errors: MUON_ERR_UNSUPPORTED_DEVICE (not sm_103), MUON_ERR_INVALID_ARG (bad
+ * config), MUON_ERR_CUDA.  Calling it again replaces the context (the old one
+ * is destroyed first).  Allocates only a few hundred bytes of device memory;
+ * the workspace is sized by the first muon_step.
+ */
+MUON_API muon_status muon_init(const muon_config* cfg);
+
+/*
+ * One Muon step over n_mats independent matrices, enqueued on `stream`.
+ *   params[i]        device float32 rows x cols, updated in place (p <- p - lr s O)
+ *   grads[i]         device float32 rows x cols, read only
+ *   momentum_bufs[i] device float32 rows x cols, updated in place (m <- m')
+ *   shapes[i]        stored shape; rows, cols >= 8 and multiples of 8
+ *   n_mats >= 0 (0 is a no-op); lr, beta as in the formulas above;
+ *   nesterov 0/1; ns_steps 0..n_coeff_rows (0 gives O = X0).
+ * The host arrays are read during the call only.  A matrix must not alias
+ * another one of the same call.  Matrices of equal oriented shape are batched
+ * into the same launches.  When the list of shapes differs from the previous
+ * call's, the workspace is rebuilt, which synchronises `stream`; otherwise the
+ * call never blocks the host.  Errors: MUON_ERR_NOT_INITIALIZED,
+ * MUON_ERR_INVALID_ARG, MUON_ERR_UNSUPPORTED_SHAPE, MUON_ERR_MISALIGNED,
+ * MUON_ERR_OUT_OF_MEMORY, MUON_ERR_CUDA.  On an argument error nothing is
+ * enqueued.
+ */
+MUON_API muon_status muon_step(float* const params[], const float* const grads[],
+                      float* const momentum_bufs[], const muon_shape shapes[], int n_mats,
+                      float lr, float beta, int nesterov, int ns_steps, muon_stream_t stream);
+
+/* Free the workspace and the context.  Synchronises the device first. */
+MUON_API muon_status muon_destroy(void);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word:
+ * MUON_OK, MUON_ERR_DEVICE_TIMEOUT or MUON_ERR_DEVICE_BOUNDS (or MUON_ERR_CUDA
+ * if the stream itself reports an error).
+ */
+MUON_API muon_status muon_get_status(muon_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+MUON_API const char* muon_status_string(muon_status s);
+
+/*
+ * Counters of the last muon_step: kernel launches it enqueued, workspace bytes,
+ * shape classes, and the algorithmic Newton-Schulz flop count
+ * (per matrix and iteration 3 m^2 n + m^3 with m <= n the oriented sides).
+ */
+typedef struct muon_step_info {
+    int launches;
+    int n_classes;
+    long long workspace_bytes;
+    double ns_alg_flops;
+    double elementwise_alg_bytes;  /* 14 B/elem momentum+norm pass + 8 B/elem weight update */
+} muon_step_info;
+MUON_API muon_status muon_get_step_info(muon_step_info* out);
+
+/*
+ * Host-only planning query (needs no device and no muon_init): validates the
+ * shapes exactly as muon_step does and describes the step it would run --
+ * oriented shape classes (matrices with equal (min side, max side,
+ * transposed) share launches), kernel launches per step, workspace bytes,
+ * algorithmic Newton-Schulz flops (3 m^2 n + m^3 per matrix and iteration),
+ * executed tensor-core flops of the 128 x 256 tiles (diagonal and ragged tiles
+ * included), algorithmic elementwise bytes (22 per element), momentum CTAs, and
+ * tiles per Gram/polynomial launch and per axpy launch.
+ * ns_steps is checked against the current context's table (16 rows without one).
+ */
+typedef struct muon_plan_info {
+    int n_classes;
+    int launches;
+    long long workspace_bytes;
+    double ns_alg_flops;
+    double ns_executed_flops;
+    double elementwise_alg_bytes;
+    int momentum_ctas;
+    long long sym_tiles;
+    long long axpy_tiles;
+} muon_plan_info;
+MUON_API muon_status muon_plan_query(const muon_shape shapes[], int n_mats, int ns_steps, muon_plan_info* out);
+
+/*
+ * Kernel timing (needs MUON_DEBUG_TIME_KERNELS): synchronises on the recorded
+ * events and returns, per kernel kind, the summed device milliseconds and the
+ * launch count since the previous call, then resets them.  Kinds:
+ * 0 momentum+norm, 1 Gram, 2 polynomial, 3 axpy, 4 axpy with fused weight
+ * update, 5 standalone weight update (ns_steps == 0).  n_kinds <= 6.
+ */
+MUON_API muon_status muon_kernel_times(double* ms_out, int* launches_out, int n_kinds);
+
+/*
+ * Test support.  muon_debug_copy_ns_output copies O of matrix `mat` of the last
+ * step (float32, stored rows x cols layout) to the device buffer dst on
+ * `stream`; needs MUON_DEBUG_KEEP_O.  muon_debug_copy_norms copies ||u||_F of
+ * the first n matrices of the last step to host memory (synchronises).
+ */
+MUON_API muon_status muon_debug_copy_ns_output(int mat, float* dst_device, muon_stream_t stream);
+MUON_API muon_status muon_debug_copy_norms(float* dst_host, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUON_H */

@@ -1,0 +1,713 @@
+// muon_api.cu -- the C ABI of libmuon.so (declared in include/muon.h) and the
+// host-side planner: argument checks, grouping of the step's matrices into
+// oriented shape classes, one workspace arena per shape list, TMA tensor maps,
+// and the launch sequence
+//   momentum_norm  ->  K x { Gram -> polynomial -> axpy (the last one fused with
+//   the weight update) }     (or the standalone update when K = 0).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <utility>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "kernels.cuh"
+
+using namespace muon;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kKinds = 6;  // momentum, gram, poly, axpy, axpy+update, update
+constexpr int kMaxCoeffRows = 16;
+
+struct ClassPlan {
+    int m = 0, n = 0, transposed = 0;
+    std::vector<int> mats;  // step indices, in step order
+    __nv_bfloat16* X[2] = {nullptr, nullptr};
+    __nv_bfloat16* A = nullptr;
+    __nv_bfloat16* B = nullptr;
+    CUtensorMap tmXk[2], tmXmn[2], tmAk, tmBk;
+    int row_blocks = 0, col_tiles = 0, sym_tiles = 0, axpy_tiles = 0;
+};
+
+struct Plan {
+    std::vector<muon_shape> shapes;
+    std::vector<ClassPlan> classes;
+    std::vector<int> mat_class, mat_slot;
+    // class-ordered step index: matrices of class 0 first, then class 1, ...
+    std::vector<int> order;         // position -> step matrix
+    std::vector<int> position;      // step matrix -> position
+    char* arena = nullptr;
+    size_t arena_bytes = 0;
+    float* inv_norm = nullptr;
+    float* norms = nullptr;
+    float* aspect = nullptr;
+    unsigned int* counters = nullptr;
+    float** p_table = nullptr;
+    float** dbg_table = nullptr;    // device array of per-matrix O buffers (KEEP_O)
+    float* partials = nullptr;
+    size_t workspace_bf16_bytes = 0;
+    char* workspace_bf16 = nullptr;
+    std::vector<float*> dbg_O;      // host copies of the O buffer pointers
+    double ns_flops_per_iter = 0.0;
+    double elem_bytes = 0.0;
+};
+
+struct PendingTime {
+    int kind;
+    cudaEvent_t a, b;
+};
+
+struct Context {
+    int device = -1;
+    int sm_count = 0;
+    std::vector<double> coeffs;
+    int n_rows = 0;
+    double eps = 1e-7;
+    int momentum_mode = 0;
+    int debug = 0;
+    unsigned long long timeout_ns = 5000000000ull;
+    EncodeTiledFn encode = nullptr;
+    unsigned int* status = nullptr;
+    Plan* plan = nullptr;
+    muon_step_info info{};
+    std::vector<cudaEvent_t> event_pool;
+    std::vector<PendingTime> pending;
+    double kind_ms[kKinds] = {0};
+    int kind_launches[kKinds] = {0};
+    bool injected = false;
+};
+
+Context* g_ctx = nullptr;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+void free_plan(Plan* p) {
+    if (!p) return;
+    if (p->arena) cudaFree(p->arena);
+    delete p;
+}
+
+muon_status encode_map(EncodeTiledFn enc, CUtensorMap* map, void* base, int cols, int rows, int depth,
+                       int box_cols, int box_rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(depth)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                             static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
+}
+
+int sym_tiles_per_mat(int row_blocks) {
+    int t = 0;
+    for (int bi = 0; bi < row_blocks; ++bi) t += (row_blocks - bi + 1) / 2;
+    return t;
+}
+
+// Host-only part of planning: shape classes, arena layout, tile counts.
+struct Layout {
+    std::vector<size_t> offX0, offX1, offA, offB, off_dbg;
+    size_t bf16_end = 0, off_inv = 0, off_nrm = 0, off_asp = 0, off_cnt = 0, off_pt = 0, off_dt = 0,
+           off_part = 0, total = 0;
+    int momentum_ctas = 0;
+    long long sym_tiles = 0, axpy_tiles = 0;
+    double ns_exec_flops_per_iter = 0.0;
+};
+
+void compute_layout(Plan* P, const muon_shape* shapes, int n, bool keep_o, Layout* L) {
+    P->shapes.assign(shapes, shapes + n);
+    P->mat_class.resize(n);
+    P->mat_slot.resize(n);
+    for (int i = 0; i < n; ++i) {
+        const int r = shapes[i].rows, c = shapes[i].cols;
+        const int tr = r > c ? 1 : 0;
+        const int m = tr ? c : r, nn = tr ? r : c;
+        int ci = -1;
+        for (size_t k = 0; k < P->classes.size(); ++k)
+            if (P->classes[k].m == m && P->classes[k].n == nn && P->classes[k].transposed == tr) {
+                ci = static_cast<int>(k);
+                break;
+            }
+        if (ci < 0) {
+            ClassPlan cp;
+            cp.m = m;
+            cp.n = nn;
+            cp.transposed = tr;
+            P->classes.push_back(cp);
+            ci = static_cast<int>(P->classes.size()) - 1;
+        }
+        P->mat_class[i] = ci;
+        P->mat_slot[i] = static_cast<int>(P->classes[ci].mats.size());
+        P->classes[ci].mats.push_back(i);
+    }
+    for (auto& cp : P->classes)
+        for (int i : cp.mats) P->order.push_back(i);
+    P->position.resize(n);
+    for (int k = 0; k < n; ++k) P->position[P->order[k]] = k;
+
+    size_t off = 0;
+    for (auto& cp : P->classes) {
+        const size_t G = cp.mats.size();
+        const size_t xb = G * static_cast<size_t>(cp.m) * cp.n * 2;
+        const size_t ab = G * static_cast<size_t>(cp.m) * cp.m * 2;
+        L->offX0.push_back(off); off = align_up(off + xb, 1024);
+        L->offX1.push_back(off); off = align_up(off + xb, 1024);
+        L->offA.push_back(off); off = align_up(off + ab, 1024);
+        L->offB.push_back(off); off = align_up(off + ab, 1024);
+        cp.row_blocks = (cp.m + kBM - 1) / kBM;
+        cp.col_tiles = (cp.n + kBN - 1) / kBN;
+        cp.sym_tiles = sym_tiles_per_mat(cp.row_blocks);
+        cp.axpy_tiles = cp.row_blocks * cp.col_tiles;
+        const double m = cp.m, nn = cp.n;
+        P->ns_flops_per_iter += static_cast<double>(G) * (3.0 * m * m * nn + m * m * m);
+        L->ns_exec_flops_per_iter += static_cast<double>(G) * 2.0 * kBM * kBN *
+            (static_cast<double>(cp.sym_tiles) * (cp.n + cp.m) + static_cast<double>(cp.axpy_tiles) * cp.m);
+        L->sym_tiles += static_cast<long long>(G) * cp.sym_tiles;
+        L->axpy_tiles += static_cast<long long>(G) * cp.axpy_tiles;
+        P->elem_bytes += static_cast<double>(G) * m * nn * 22.0;
+    }
+    L->bf16_end = off;
+    L->off_inv = off; off = align_up(off + n * sizeof(float), 256);
+    L->off_nrm = off; off = align_up(off + n * sizeof(float), 256);
+    L->off_asp = off; off = align_up(off + n * sizeof(float), 256);
+    L->off_cnt = off; off = align_up(off + n * sizeof(unsigned int), 256);
+    L->off_pt = off; off = align_up(off + n * sizeof(float*), 256);
+    L->off_dt = off; off = align_up(off + n * sizeof(float*), 256);
+    // one partial per momentum CTA of the largest launch chunk
+    size_t max_tiles = 0, chunk_tiles = 0;
+    for (int k = 0; k < n; ++k) {
+        if (k % kMomentumMaxMats == 0) chunk_tiles = 0;
+        const muon_shape& s = shapes[P->order[k]];
+        const size_t t = static_cast<size_t>((s.rows + kMomTile - 1) / kMomTile) *
+                         ((s.cols + kMomTile - 1) / kMomTile);
+        chunk_tiles += t;
+        L->momentum_ctas += static_cast<int>(t);
+        if (chunk_tiles > max_tiles) max_tiles = chunk_tiles;
+    }
+    L->off_part = off; off = align_up(off + max_tiles * sizeof(float), 256);
+    if (keep_o) {
+        for (int i = 0; i < n; ++i) {
+            L->off_dbg.push_back(off);
+            off = align_up(off + static_cast<size_t>(shapes[i].rows) * shapes[i].cols * sizeof(float), 256);
+        }
+    }
+    L->total = off;
+}
+
+int launches_for(const Plan* P, int ns_steps) {
+    const int n = static_cast<int>(P->shapes.size());
+    const int chunks = (n + kMomentumMaxMats - 1) / kMomentumMaxMats;
+    const int groups = (static_cast<int>(P->classes.size()) + kMaxClasses - 1) / kMaxClasses;
+    return ns_steps == 0 ? 2 * chunks : chunks + 3 * ns_steps * groups;
+}
+
+muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out) {
+    Plan* P = new Plan();
+    Layout L;
+    compute_layout(P, shapes, n, (ctx->debug & MUON_DEBUG_KEEP_O) != 0, &L);
+    P->arena_bytes = L.total;
+    if (cudaMalloc(&P->arena, L.total) != cudaSuccess) {
+        cudaGetLastError();
+        P->arena = nullptr;
+        free_plan(P);
+        return MUON_ERR_OUT_OF_MEMORY;
+    }
+    char* a = P->arena;
+    P->workspace_bf16 = a;
+    P->workspace_bf16_bytes = L.bf16_end;
+    for (size_t k = 0; k < P->classes.size(); ++k) {
+        ClassPlan& cp = P->classes[k];
+        cp.X[0] = reinterpret_cast<__nv_bfloat16*>(a + L.offX0[k]);
+        cp.X[1] = reinterpret_cast<__nv_bfloat16*>(a + L.offX1[k]);
+        cp.A = reinterpret_cast<__nv_bfloat16*>(a + L.offA[k]);
+        cp.B = reinterpret_cast<__nv_bfloat16*>(a + L.offB[k]);
+        const int G = static_cast<int>(cp.mats.size());
+        muon_status st = MUON_OK;
+        for (int pp = 0; pp < 2 && st == MUON_OK; ++pp) {
+            st = encode_map(ctx->encode, &cp.tmXk[pp], cp.X[pp], cp.n, cp.m, G, kBK, kBM);
+            if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmXmn[pp], cp.X[pp], cp.n, cp.m, G, 64, kBK);
+        }
+        if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmAk, cp.A, cp.m, cp.m, G, kBK, kBM);
+        if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmBk, cp.B, cp.m, cp.m, G, kBK, kBM);
+        if (st != MUON_OK) {
+            free_plan(P);
+            return st;
+        }
+    }
+    P->inv_norm = reinterpret_cast<float*>(a + L.off_inv);
+    P->norms = reinterpret_cast<float*>(a + L.off_nrm);
+    P->aspect = reinterpret_cast<float*>(a + L.off_asp);
+    P->counters = reinterpret_cast<unsigned int*>(a + L.off_cnt);
+    P->p_table = reinterpret_cast<float**>(a + L.off_pt);
+    P->dbg_table = reinterpret_cast<float**>(a + L.off_dt);
+    P->partials = reinterpret_cast<float*>(a + L.off_part);
+
+    // per-matrix constants, indexed by class-ordered position
+    std::vector<float> asp(n);
+    std::vector<float*> dbg(n, nullptr);
+    for (int k = 0; k < n; ++k) {
+        const muon_shape& s = shapes[P->order[k]];
+        const double ratio = static_cast<double>(s.rows) / s.cols;
+        asp[k] = static_cast<float>(std::sqrt(ratio > 1.0 ? ratio : 1.0));
+        if (!L.off_dbg.empty()) dbg[k] = reinterpret_cast<float*>(a + L.off_dbg[P->order[k]]);
+    }
+    P->dbg_O.assign(n, nullptr);
+    for (int i = 0; i < n; ++i)
+        if (!L.off_dbg.empty()) P->dbg_O[i] = reinterpret_cast<float*>(a + L.off_dbg[i]);
+    bool ok = cudaMemcpy(P->aspect, asp.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(P->dbg_table, dbg.data(), n * sizeof(float*), cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemset(P->counters, 0, n * sizeof(unsigned int)) == cudaSuccess;
+    ok = ok && cudaMemset(P->inv_norm, 0, n * sizeof(float)) == cudaSuccess;
+    ok = ok && cudaMemset(P->norms, 0, n * sizeof(float)) == cudaSuccess;
+    if (!ok) {
+        free_plan(P);
+        return MUON_ERR_CUDA;
+    }
+    *out = P;
+    return MUON_OK;
+}
+
+muon_status check_shapes(const muon_shape* shapes, int n) {
+    for (int i = 0; i < n; ++i) {
+        const int r = shapes[i].rows, c = shapes[i].cols;
+        if (r < 8 || c < 8 || (r % 8) != 0 || (c % 8) != 0 || r > 65536 || c > 65536)
+            return MUON_ERR_UNSUPPORTED_SHAPE;
+    }
+    return MUON_OK;
+}
+
+bool same_shapes(const Plan* P, const muon_shape* shapes, int n) {
+    if (!P || static_cast<int>(P->shapes.size()) != n) return false;
+    for (int i = 0; i < n; ++i)
+        if (P->shapes[i].rows != shapes[i].rows || P->shapes[i].cols != shapes[i].cols) return false;
+    return true;
+}
+
+cudaEvent_t take_event(Context* ctx) {
+    if (!ctx->event_pool.empty()) {
+        cudaEvent_t e = ctx->event_pool.back();
+        ctx->event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Runs `launch` on `stream`, bracketed by timing events when enabled.
+template <typename F>
+muon_status timed_launch(Context* ctx, int kind, cudaStream_t stream, F&& launch) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    const bool timing = (ctx->debug & MUON_DEBUG_TIME_KERNELS) != 0;
+    if (timing) {
+        a = take_event(ctx);
+        b = take_event(ctx);
+        cudaEventRecord(a, stream);
+    }
+    const cudaError_t e = launch();
+    if (timing) {
+        cudaEventRecord(b, stream);
+        ctx->pending.push_back({kind, a, b});
+    }
+    ctx->info.launches += 1;
+    return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+void fill_momentum_mat(const Plan* P, int pos, float* const params[], const float* const grads[],
+                       float* const moms[], int tile_begin, MomentumMat* M) {
+    const int i = P->order[pos];
+    const ClassPlan& cp = P->classes[P->mat_class[i]];
+    M->g = grads[i];
+    M->mom = moms[i];
+    M->p = params[i];
+    M->x0 = cp.X[0] + static_cast<size_t>(P->mat_slot[i]) * cp.m * cp.n;
+    M->rows = P->shapes[i].rows;
+    M->cols = P->shapes[i].cols;
+    M->transposed = cp.transposed;
+    M->tiles_x = (M->cols + kMomTile - 1) / kMomTile;
+    M->ntiles = M->tiles_x * ((M->rows + kMomTile - 1) / kMomTile);
+    M->tile_begin = tile_begin;
+    M->gidx = pos;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* muon_status_string(muon_status s) {
+    switch (s) {
+        case MUON_OK: return "ok";
+        case MUON_ERR_INVALID_ARG: return "invalid argument";
+        case MUON_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (rows and cols must be >= 8 and multiples of 8)";
+        case MUON_ERR_MISALIGNED: return "matrix pointer not 16-byte aligned";
+        case MUON_ERR_NOT_INITIALIZED: return "muon_init has not succeeded";
+        case MUON_ERR_CUDA: return "CUDA call failed";
+        case MUON_ERR_OUT_OF_MEMORY: return "workspace allocation failed";
+        case MUON_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
+        case MUON_ERR_DEVICE_BOUNDS: return "a kernel saw an out-of-range tile";
+        case MUON_ERR_UNSUPPORTED_DEVICE: return "no sm_103 CUDA device";
+    }
+    return "unknown status";
+}
+
+muon_status muon_destroy(void) {
+    if (!g_ctx) return MUON_OK;
+    cudaDeviceSynchronize();
+    free_plan(g_ctx->plan);
+    for (auto& pt : g_ctx->pending) {
+        cudaEventDestroy(pt.a);
+        cudaEventDestroy(pt.b);
+    }
+    for (auto e : g_ctx->event_pool) cudaEventDestroy(e);
+    if (g_ctx->status) cudaFree(g_ctx->status);
+    delete g_ctx;
+    g_ctx = nullptr;
+    return MUON_OK;
+}
+
+muon_status muon_init(const muon_config* cfg) {
+    // validate the configuration before touching the device
+    std::vector<double> coeffs;
+    if (cfg && cfg->coeffs) {
+        if (cfg->n_coeff_rows < 1 || cfg->n_coeff_rows > kMaxCoeffRows) return MUON_ERR_INVALID_ARG;
+        coeffs.assign(cfg->coeffs, cfg->coeffs + 3 * cfg->n_coeff_rows);
+        for (double v : coeffs)
+            if (!std::isfinite(v)) return MUON_ERR_INVALID_ARG;
+    } else {
+        for (int k = 0; k < 5; ++k) {
+            coeffs.push_back(3.4445);
+            coeffs.push_back(-4.7750);
+            coeffs.push_back(2.0315);
+        }
+    }
+    if (cfg && cfg->momentum_mode != MUON_MOMENTUM_SGD_NESTEROV && cfg->momentum_mode != MUON_MOMENTUM_EMA)
+        return MUON_ERR_INVALID_ARG;
+    if (cfg && !(std::isfinite(cfg->eps) && std::isfinite(cfg->wait_timeout_s))) return MUON_ERR_INVALID_ARG;
+
+    muon_destroy();
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MUON_ERR_UNSUPPORTED_DEVICE;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MUON_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (!(prop.major == 10 && prop.minor == 3)) return MUON_ERR_UNSUPPORTED_DEVICE;
+
+    Context* ctx = new Context();
+    ctx->device = dev;
+    ctx->sm_count = prop.multiProcessorCount;
+    ctx->coeffs = coeffs;
+    ctx->n_rows = static_cast<int>(coeffs.size() / 3);
+    if (cfg) {
+        if (cfg->eps > 0) ctx->eps = cfg->eps;
+        ctx->momentum_mode = cfg->momentum_mode;
+        ctx->debug = cfg->debug_flags;
+        if (cfg->wait_timeout_s > 0)
+            ctx->timeout_ns = static_cast<unsigned long long>(cfg->wait_timeout_s * 1e9);
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        delete ctx;
+        return MUON_ERR_CUDA;
+    }
+    ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (ns_gemm_prepare() != cudaSuccess ||
+        cudaMalloc(&ctx->status, sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemset(ctx->status, 0, sizeof(unsigned int)) != cudaSuccess) {
+        cudaGetLastError();
+        if (ctx->status) cudaFree(ctx->status);
+        delete ctx;
+        return MUON_ERR_CUDA;
+    }
+    g_ctx = ctx;
+    return MUON_OK;
+}
+
+muon_status muon_step(float* const params[], const float* const grads[], float* const momentum_bufs[],
+                      const muon_shape shapes[], int n_mats, float lr, float beta, int nesterov,
+                      int ns_steps, muon_stream_t stream_) {
+    Context* ctx = g_ctx;
+    if (!ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (n_mats < 0) return MUON_ERR_INVALID_ARG;
+    if (n_mats == 0) {
+        ctx->info = muon_step_info{};
+        return MUON_OK;
+    }
+    if (!params || !grads || !momentum_bufs || !shapes) return MUON_ERR_INVALID_ARG;
+    if (ns_steps < 0 || ns_steps > ctx->n_rows) return MUON_ERR_INVALID_ARG;
+    if (!std::isfinite(lr) || !std::isfinite(beta)) return MUON_ERR_INVALID_ARG;
+    if (check_shapes(shapes, n_mats) != MUON_OK) return MUON_ERR_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < n_mats; ++i) {
+        if (!params[i] || !grads[i] || !momentum_bufs[i]) return MUON_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(params[i]) | reinterpret_cast<uintptr_t>(grads[i]) |
+             reinterpret_cast<uintptr_t>(momentum_bufs[i])) & 15u)
+            return MUON_ERR_MISALIGNED;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    if (!same_shapes(ctx->plan, shapes, n_mats)) {
+        if (ctx->plan) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+            free_plan(ctx->plan);
+            ctx->plan = nullptr;
+        }
+        Plan* P = nullptr;
+        const muon_status st = build_plan(ctx, shapes, n_mats, &P);
+        if (st != MUON_OK) return st;
+        ctx->plan = P;
+    }
+    Plan* P = ctx->plan;
+    ctx->info = muon_step_info{};
+    ctx->info.n_classes = static_cast<int>(P->classes.size());
+    ctx->info.workspace_bytes = static_cast<long long>(P->arena_bytes);
+    ctx->info.ns_alg_flops = P->ns_flops_per_iter * ns_steps;
+    ctx->info.elementwise_alg_bytes = P->elem_bytes;
+
+    if (ctx->debug & MUON_DEBUG_POISON_WORKSPACE) {
+        if (cudaMemsetAsync(P->workspace_bf16, 0xFF, P->workspace_bf16_bytes, stream) != cudaSuccess)
+            return MUON_ERR_CUDA;
+    }
+
+    // ---- momentum + norm (chunks of kMomentumMaxMats matrices, class order)
+    static MomentumParams mp;  // ~12 KiB: kept off the stack
+    for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
+        const int cnt = std::min(kMomentumMaxMats, n_mats - base);
+        std::memset(&mp, 0, sizeof(mp));
+        int tiles = 0;
+        for (int k = 0; k < cnt; ++k) {
+            fill_momentum_mat(P, base + k, params, grads, momentum_bufs, tiles, &mp.mats[k]);
+            tiles += mp.mats[k].ntiles;
+        }
+        mp.nmats = cnt;
+        mp.total_tiles = tiles;
+        mp.beta = beta;
+        mp.nesterov = nesterov ? 1 : 0;
+        mp.mode = ctx->momentum_mode;
+        mp.eps = static_cast<float>(ctx->eps);
+        mp.partials = P->partials;
+        mp.counters = P->counters;
+        mp.inv_norm = P->inv_norm;
+        mp.norms = P->norms;
+        mp.p_table = P->p_table;
+        const muon_status st = timed_launch(ctx, 0, stream, [&] { return launch_momentum_norm(mp, stream); });
+        if (st != MUON_OK) return st;
+    }
+
+    const bool keep_o = (ctx->debug & MUON_DEBUG_KEEP_O) != 0;
+    if (ns_steps == 0) {
+        static UpdateParams up;
+        for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
+            const int cnt = std::min(kMomentumMaxMats, n_mats - base);
+            std::memset(&up, 0, sizeof(up));
+            int tiles = 0;
+            for (int k = 0; k < cnt; ++k) {
+                fill_momentum_mat(P, base + k, params, grads, momentum_bufs, tiles, &up.mats[k]);
+                tiles += up.mats[k].ntiles;
+            }
+            up.nmats = cnt;
+            up.total_tiles = tiles;
+            up.inv_norm = P->inv_norm;
+            up.aspect = P->aspect;
+            up.lr = lr;
+            up.dbg_O = keep_o ? P->dbg_table : nullptr;
+            const muon_status st = timed_launch(ctx, 5, stream, [&] { return launch_update(up, stream); });
+            if (st != MUON_OK) return st;
+        }
+        return MUON_OK;
+    }
+
+    // ---- Newton-Schulz iterations: per group of <= kMaxClasses classes
+    static GemmParams gp;
+    const int nclass = static_cast<int>(P->classes.size());
+    for (int it = 0; it < ns_steps; ++it) {
+        const double* row = &ctx->coeffs[3 * it];
+        const int pin = it & 1, pout = pin ^ 1;
+        const bool last = (it == ns_steps - 1);
+        for (int g0 = 0; g0 < nclass; g0 += kMaxClasses) {
+            const int gc = std::min(kMaxClasses, nclass - g0);
+            for (int mode = MODE_GRAM; mode <= MODE_AXPY; ++mode) {
+                std::memset(&gp, 0, sizeof(gp));
+                const int eff_mode = (mode == MODE_AXPY && last) ? MODE_AXPY_FINAL : mode;
+                gp.mode = eff_mode;
+                gp.nclasses = gc;
+                gp.first_iter = (it == 0 && mode != MODE_POLY) ? 1 : 0;
+                gp.ca = static_cast<float>(row[0]);
+                gp.cb = static_cast<float>(row[1]);
+                gp.cc = static_cast<float>(row[2]);
+                gp.inv_norm = P->inv_norm;
+                gp.aspect = P->aspect;
+                gp.lr = lr;
+                gp.p_table = P->p_table;
+                gp.dbg_O = keep_o ? P->dbg_table : nullptr;
+                gp.status = ctx->status;
+                gp.timeout_ns = ctx->timeout_ns;
+                gp.inject_lost_load = ((ctx->debug & MUON_DEBUG_INJECT_LOST_LOAD) && !ctx->injected &&
+                                       it == 0 && mode == MODE_GRAM && g0 == 0)
+                                          ? 1
+                                          : 0;
+                if (gp.inject_lost_load) ctx->injected = true;
+                int tiles = 0;
+                int mat_base = 0;
+                for (int k = 0; k < g0; ++k) mat_base += static_cast<int>(P->classes[k].mats.size());
+                for (int k = 0; k < gc; ++k) {
+                    const ClassPlan& cp = P->classes[g0 + k];
+                    GemmClass& C = gp.cls[k];
+                    const int G = static_cast<int>(cp.mats.size());
+                    C.m = cp.m;
+                    C.n = cp.n;
+                    C.nmats = G;
+                    C.tile_begin = tiles;
+                    C.row_blocks = cp.row_blocks;
+                    C.col_tiles = cp.col_tiles;
+                    C.transposed = cp.transposed;
+                    C.mat_base = mat_base;
+                    if (mode == MODE_GRAM) {
+                        C.tiles_per_mat = cp.sym_tiles;
+                        C.k_blocks = (cp.n + kBK - 1) / kBK;
+                        C.aux = nullptr;
+                        C.out = cp.A;
+                        gp.tmA[k] = cp.tmXk[pin];
+                        gp.tmB[k] = cp.tmXk[pin];
+                    } else if (mode == MODE_POLY) {
+                        C.tiles_per_mat = cp.sym_tiles;
+                        C.k_blocks = (cp.m + kBK - 1) / kBK;
+                        C.aux = cp.A;
+                        C.out = cp.B;
+                        gp.tmA[k] = cp.tmAk;
+                        gp.tmB[k] = cp.tmAk;
+                    } else {
+                        C.tiles_per_mat = cp.axpy_tiles;
+                        C.k_blocks = (cp.m + kBK - 1) / kBK;
+                        C.aux = cp.X[pin];
+                        C.out = cp.X[pout];
+                        gp.tmA[k] = cp.tmBk;
+                        gp.tmB[k] = cp.tmXmn[pin];
+                    }
+                    tiles += C.tiles_per_mat * G;
+                    mat_base += G;
+                }
+                gp.total_tiles = tiles;
+                const int grid = std::min(tiles, ctx->sm_count);
+                const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3 : 4;
+                const muon_status st = timed_launch(ctx, kind, stream, [&] { return launch_ns_gemm(gp, grid, stream); });
+                if (st != MUON_OK) return st;
+            }
+        }
+    }
+    return MUON_OK;
+}
+
+muon_status muon_plan_query(const muon_shape shapes[], int n_mats, int ns_steps, muon_plan_info* out) {
+    if (!out || n_mats < 0 || (n_mats > 0 && !shapes)) return MUON_ERR_INVALID_ARG;
+    const int max_rows = g_ctx ? g_ctx->n_rows : kMaxCoeffRows;
+    if (ns_steps < 0 || ns_steps > max_rows) return MUON_ERR_INVALID_ARG;
+    if (check_shapes(shapes, n_mats) != MUON_OK) return MUON_ERR_UNSUPPORTED_SHAPE;
+    std::memset(out, 0, sizeof(*out));
+    if (n_mats == 0) return MUON_OK;
+    Plan P;
+    Layout L;
+    compute_layout(&P, shapes, n_mats, g_ctx && (g_ctx->debug & MUON_DEBUG_KEEP_O), &L);
+    out->n_classes = static_cast<int>(P.classes.size());
+    out->launches = launches_for(&P, ns_steps);
+    out->workspace_bytes = static_cast<long long>(L.total);
+    out->ns_alg_flops = P.ns_flops_per_iter * ns_steps;
+    out->ns_executed_flops = L.ns_exec_flops_per_iter * ns_steps;
+    out->elementwise_alg_bytes = P.elem_bytes;
+    out->momentum_ctas = L.momentum_ctas;
+    out->sym_tiles = L.sym_tiles;
+    out->axpy_tiles = L.axpy_tiles;
+    return MUON_OK;
+}
+
+muon_status muon_get_status(muon_stream_t stream) {
+    Context* ctx = g_ctx;
+    if (!ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
+    unsigned int st = 0;
+    if (cudaMemcpy(&st, ctx->status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+    if (st != 0 && cudaMemset(ctx->status, 0, sizeof(unsigned int)) != cudaSuccess) return MUON_ERR_CUDA;
+    if (st & STATUS_TIMEOUT) return MUON_ERR_DEVICE_TIMEOUT;
+    if (st & STATUS_BOUNDS) return MUON_ERR_DEVICE_BOUNDS;
+    return MUON_OK;
+}
+
+muon_status muon_get_step_info(muon_step_info* out) {
+    if (!g_ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (!out) return MUON_ERR_INVALID_ARG;
+    *out = g_ctx->info;
+    return MUON_OK;
+}
+
+muon_status muon_kernel_times(double* ms_out, int* launches_out, int n_kinds) {
+    Context* ctx = g_ctx;
+    if (!ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (n_kinds < 0 || n_kinds > kKinds || (n_kinds > 0 && (!ms_out || !launches_out)))
+        return MUON_ERR_INVALID_ARG;
+    muon_status result = MUON_OK;
+    for (auto& pt : ctx->pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(pt.b) != cudaSuccess || cudaEventElapsedTime(&ms, pt.a, pt.b) != cudaSuccess) {
+            cudaGetLastError();
+            result = MUON_ERR_CUDA;
+        }
+        ctx->kind_ms[pt.kind] += ms;
+        ctx->kind_launches[pt.kind] += 1;
+        ctx->event_pool.push_back(pt.a);
+        ctx->event_pool.push_back(pt.b);
+    }
+    ctx->pending.clear();
+    for (int k = 0; k < n_kinds; ++k) {
+        ms_out[k] = ctx->kind_ms[k];
+        launches_out[k] = ctx->kind_launches[k];
+    }
+    for (int k = 0; k < kKinds; ++k) {
+        ctx->kind_ms[k] = 0;
+        ctx->kind_launches[k] = 0;
+    }
+    return result;
+}
+
+muon_status muon_debug_copy_ns_output(int mat, float* dst_device, muon_stream_t stream) {
+    Context* ctx = g_ctx;
+    if (!ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (!(ctx->debug & MUON_DEBUG_KEEP_O) || !ctx->plan || !dst_device) return MUON_ERR_INVALID_ARG;
+    Plan* P = ctx->plan;
+    if (mat < 0 || mat >= static_cast<int>(P->shapes.size())) return MUON_ERR_INVALID_ARG;
+    const size_t bytes = static_cast<size_t>(P->shapes[mat].rows) * P->shapes[mat].cols * sizeof(float);
+    return cudaMemcpyAsync(dst_device, P->dbg_O[mat], bytes, cudaMemcpyDeviceToDevice,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MUON_OK
+               : MUON_ERR_CUDA;
+}
+
+muon_status muon_debug_copy_norms(float* dst_host, int n) {
+    Context* ctx = g_ctx;
+    if (!ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (!ctx->plan || !dst_host || n < 0 || n > static_cast<int>(ctx->plan->shapes.size()))
+        return MUON_ERR_INVALID_ARG;
+    Plan* P = ctx->plan;
+    std::vector<float> tmp(P->shapes.size());
+    if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
+    if (cudaMemcpy(tmp.data(), P->norms, tmp.size() * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MUON_ERR_CUDA;
+    for (int i = 0; i < n; ++i) dst_host[i] = tmp[P->position[i]];
+    return MUON_OK;
+}
+
+}  // extern "C"

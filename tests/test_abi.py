@@ -1,0 +1,146 @@
+"""The C ABI on the CPU: libmuon.so loads, exports every function include/muon.h
+declares, validates arguments, and its host-only planner counts work the way
+the tiling defines it (checked against an independent enumeration here)."""
+import ctypes
+import math
+
+import pytest
+import torch
+
+import pretraining_optimizer_step_b300 as mu
+import workloads
+
+
+@pytest.fixture(scope="module")
+def L():
+    return mu.lib()
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = mu.declared_symbols()
+    assert len(names) >= 10
+    raw = ctypes.CDLL(mu.LIB_PATH)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_library_hides_internal_symbols():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", mu.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(mu.declared_symbols()) <= exported
+    assert not [s for s in exported if "launch_ns_gemm" in s or "compute_layout" in s]
+
+
+def test_status_strings(L):
+    for code in range(0, 10):
+        s = mu.muon_status_string(code)
+        assert s and s != "unknown status"
+    assert mu.muon_status_string(1234) == "unknown status"
+
+
+def test_step_before_init_is_rejected(L):
+    mu.muon_destroy()
+    args = mu.StepArgs([16], [16], [16], shapes=[(8, 8)])
+    assert mu.muon_step(args, check=False) == mu.MUON_ERR_NOT_INITIALIZED
+    assert mu.muon_get_status(check=False) == mu.MUON_ERR_NOT_INITIALIZED
+    assert mu.lib().muon_get_step_info(None) == mu.MUON_ERR_NOT_INITIALIZED
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_init_without_gpu_reports_unsupported_device(L):
+    assert mu.muon_init(check=False) == mu.MUON_ERR_UNSUPPORTED_DEVICE
+
+
+def test_init_rejects_bad_configs_before_touching_the_device(L):
+    assert mu.muon_init(momentum_mode=7, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_init(coeffs=[(1.0, float("nan"), 0.0)], check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_init(coeffs=[(1.0, 0.0, 0.0)] * 17, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_init(eps=float("inf"), check=False) == mu.MUON_ERR_INVALID_ARG
+    cfg = mu.muon_config()
+    cfg.coeffs = (ctypes.c_double * 3)(1.0, 0.0, 0.0)
+    cfg.n_coeff_rows = 0
+    assert L.muon_init(ctypes.byref(cfg)) == mu.MUON_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ host planner
+def enumerate_tiles(m, n):
+    """Brute-force tile sets of the 128 x 256 tiling: Gram/polynomial tiles cover
+    every 128 x 128 block on or above the diagonal exactly once (tile = row block
+    bi, column blocks cb and cb + 1 for cb = bi, bi + 2, ...); axpy tiles cover X."""
+    rb = math.ceil(m / 128)
+    sym = [(bi, cb) for bi in range(rb) for cb in range(bi, rb, 2)]
+    covered = set()
+    for bi, cb in sym:
+        for c in (cb, cb + 1):
+            if c < rb:
+                assert (bi, c) not in covered
+                covered.add((bi, c))
+    assert covered == {(i, j) for i in range(rb) for j in range(i, rb)}
+    axpy = rb * math.ceil(n / 256)
+    return len(sym), axpy
+
+
+def expected_plan(shapes, K):
+    classes = {}
+    for r, c in shapes:
+        key = (min(r, c), max(r, c), r > c)
+        classes[key] = classes.get(key, 0) + 1
+    alg = exe = 0.0
+    sym = axpy = 0
+    for (m, n, _), G in classes.items():
+        s, a = enumerate_tiles(m, n)
+        sym += G * s
+        axpy += G * a
+        alg += G * K * (3 * m * m * n + m ** 3)
+        exe += G * K * 2 * 128 * 256 * (s * (n + m) + a * m)
+    ctas = sum(math.ceil(r / 64) * math.ceil(c / 64) for r, c in shapes)
+    elem = sum(22 * r * c for r, c in shapes)
+    return len(classes), alg, exe, sym, axpy, ctas, elem
+
+
+@pytest.mark.parametrize("name", ["d2", "d12", "d20", "d26", "sweep_1024_tall", "sweep_256_sq"])
+def test_plan_query_counts(L, name):
+    shapes = workloads.config_shapes(name)
+    q = mu.muon_plan_query(shapes, ns_steps=5)
+    ncls, alg, exe, sym, axpy, ctas, elem = expected_plan(shapes, 5)
+    assert q["n_classes"] == ncls
+    assert q["ns_alg_flops"] == pytest.approx(alg, rel=1e-12)
+    assert q["ns_executed_flops"] == pytest.approx(exe, rel=1e-12)
+    assert q["sym_tiles"] == sym and q["axpy_tiles"] == axpy
+    assert q["momentum_ctas"] == ctas
+    assert q["elementwise_alg_bytes"] == pytest.approx(elem, rel=1e-12)
+    assert q["launches"] == 1 + 3 * 5 * math.ceil(ncls / 8)
+    ws_min = sum(2 * (2 * min(r, c) * max(r, c) + 2 * min(r, c) ** 2) for r, c in shapes)
+    assert q["workspace_bytes"] >= ws_min
+
+
+def test_plan_query_d26_headline_numbers(L):
+    q = mu.muon_plan_query(workloads.config_shapes("d26"), ns_steps=5)
+    assert q["n_classes"] == 3                     # square, tall (transposed), wide
+    assert q["ns_alg_flops"] == pytest.approx(2.516e13, rel=1e-3)
+    assert q["elementwise_alg_bytes"] == pytest.approx(1.90e10, rel=1e-2)
+    assert 1.0 < q["ns_executed_flops"] / q["ns_alg_flops"] < 1.3
+
+
+def test_plan_query_validation(L):
+    assert mu.muon_plan_query([(7, 8)], check=False) == mu.MUON_ERR_UNSUPPORTED_SHAPE
+    assert mu.muon_plan_query([(12, 16)], check=False) == mu.MUON_ERR_UNSUPPORTED_SHAPE
+    assert mu.muon_plan_query([(8, 0)], check=False) == mu.MUON_ERR_UNSUPPORTED_SHAPE
+    assert mu.muon_plan_query([(8, 65544)], check=False) == mu.MUON_ERR_UNSUPPORTED_SHAPE
+    assert mu.muon_plan_query([(8, 8)], ns_steps=-1, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_plan_query([(8, 8)], ns_steps=17, check=False) == mu.MUON_ERR_INVALID_ARG
+    info = mu.muon_plan_info()
+    assert L.muon_plan_query(None, -1, 5, ctypes.byref(info)) == mu.MUON_ERR_INVALID_ARG
+    assert L.muon_plan_query(None, 1, 5, ctypes.byref(info)) == mu.MUON_ERR_INVALID_ARG
+    q = mu.muon_plan_query([], ns_steps=5)
+    assert q["launches"] == 0 and q["workspace_bytes"] == 0
+
+
+def test_plan_query_ns0_and_class_limit(L):
+    q = mu.muon_plan_query([(64, 64)], ns_steps=0)
+    assert q["launches"] == 2 and q["ns_alg_flops"] == 0
+    # nine distinct shape classes need two launch groups per mode
+    shapes = [(8 * (k + 1), 64) for k in range(9)]
+    q = mu.muon_plan_query(shapes, ns_steps=2)
+    assert q["n_classes"] == 9 and q["launches"] == 1 + 3 * 2 * 2

@@ -1,0 +1,198 @@
+"""Parity of the CUDA Muon step (through the C ABI) with the fp64 oracle.
+
+Every case draws seeded inputs from workloads.py on the device, keeps a CPU copy
+of them, runs one muon_step, and compares each checked matrix with the oracle
+run on the same CPU copy (tolerances in tests/gpu_util.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pretraining_optimizer_step_b300 as mu
+import workloads
+from gpu_util import TOL_O, check_matrix, rel_fro, run_gpu_step
+
+pytestmark = pytest.mark.gpu
+
+DEFAULT = oracle.DEFAULT_COEFFS
+
+
+@pytest.fixture(autouse=True)
+def fresh_context():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mu.muon_init(debug_flags=mu.MUON_DEBUG_KEEP_O, wait_timeout_s=2.0)
+    yield
+    mu.muon_destroy()
+
+
+def cpu_copy(ts):
+    return [t.detach().cpu().numpy().copy() for t in ts]
+
+
+def run_and_check(params, grads, moms, check_idx=None, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
+                  coeffs=DEFAULT, mode=0, tol_o=None):
+    """tol_o: None (2e-2), a number, or a function of the stored shape."""
+    p0, g0, m0 = cpu_copy(params), cpu_copy(grads), cpu_copy(moms)
+    O = run_gpu_step(params, grads, moms, lr=lr, beta=beta, nesterov=nesterov, ns_steps=ns_steps)
+    norms = mu.muon_debug_copy_norms(len(params))
+    p1, m1 = cpu_copy(params), cpu_copy(moms)
+    idx = range(len(params)) if check_idx is None else check_idx
+    worst = {}
+    for i in idx:
+        tol = TOL_O if tol_o is None else (tol_o(p0[i].shape) if callable(tol_o) else tol_o)
+        rep, _ = check_matrix(i, p0[i], g0[i], m0[i], p1[i], m1[i], O[i], lr, beta, nesterov, ns_steps,
+                              coeffs, mode=mode, norm_gpu=norms[i], tol_o=tol)
+        for k, v in rep.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    return worst
+
+
+def test_d2_full_stack():
+    p, g, m, _ = workloads.make_stack("d2", "cuda")
+    worst = run_and_check(p, g, m)
+    assert worst["O"] < TOL_O
+
+
+@pytest.mark.parametrize("ns_steps", [0, 1, 2])
+def test_d2_short_iterations(ns_steps):
+    p, g, m, _ = workloads.make_stack("d2", "cuda")
+    run_and_check(p, g, m, ns_steps=ns_steps)
+
+
+RAGGED = [(136, 200), (200, 136), (8, 8), (8, 1024), (1024, 8), (264, 264), (128, 384), (384, 128),
+          (520, 64), (392, 1032), (1032, 392)]
+
+
+def small_side_tol(shape):
+    # below 64 rows or columns the Frobenius error of bf16 arithmetic does not
+    # average out: over 40 seeded 8 x 8 inputs, the kernels' rounding points
+    # give O errors up to 3.5e-2 against the fp64 oracle (median 1.6e-2)
+    return TOL_O if min(shape) >= 64 else 6e-2
+
+
+@pytest.mark.parametrize("ns_steps,tol", [(1, 5e-3), (5, small_side_tol)])
+def test_ragged_and_edge_shapes(ns_steps, tol):
+    # one iteration is checked tightly (bf16 rounding of X0 gives about 1.7e-3),
+    # so any tile, mask or transpose error shows as an O(1) mismatch
+    p, g, m, _ = workloads.make_custom(RAGGED, "cuda", tag="ragged")
+    run_and_check(p, g, m, ns_steps=ns_steps, tol_o=tol)
+
+
+@pytest.mark.parametrize("nesterov,mode", [(False, 0), (True, 1), (False, 1)])
+def test_momentum_variants(nesterov, mode):
+    mu.muon_destroy()
+    mu.muon_init(debug_flags=mu.MUON_DEBUG_KEEP_O, momentum_mode=mode, wait_timeout_s=2.0)
+    p, g, m, _ = workloads.make_stack("d2", "cuda")
+    run_and_check(p, g, m, nesterov=nesterov, beta=0.9, lr=0.05, mode=mode)
+
+
+@pytest.mark.parametrize("ns_steps,tol", [(2, TOL_O), (5, 0.2)])
+def test_pages_polar_express_rows(ns_steps, tol):
+    # the two rows the pages print, followed by the default row.  Their own two
+    # iterations stay within 2e-2 (bf16 gives about 3.4e-3); continuing with the
+    # default row from their output amplifies bf16 rounding (the composite map
+    # is steep there): about 0.11 at five iterations for the kernels' rounding
+    # points, hence the wider bound there
+    rows = [tuple(r) for r in oracle.PAGES_POLAR_EXPRESS_ROWS] + [oracle.DEFAULT_ROW] * 3
+    mu.muon_destroy()
+    mu.muon_init(coeffs=rows, debug_flags=mu.MUON_DEBUG_KEEP_O, wait_timeout_s=2.0)
+    p, g, m, _ = workloads.make_stack("d2", "cuda")
+    run_and_check(p, g, m, coeffs=np.array(rows), ns_steps=ns_steps, tol_o=tol)
+
+
+def test_d12_stack_sampled():
+    p, g, m, _ = workloads.make_stack("d12", "cuda")
+    run_and_check(p, g, m, check_idx=[0, 3, 4, 5, 64, 70, 71])
+
+
+def test_zero_gradient_and_momentum():
+    shapes = [(64, 64), (256, 64), (64, 256)]
+    p = [torch.randn(s, device="cuda") for s in shapes]
+    g = [torch.zeros(s, device="cuda") for s in shapes]
+    m = [torch.zeros(s, device="cuda") for s in shapes]
+    p0 = [t.clone() for t in p]
+    O = run_gpu_step(p, g, m)
+    for i in range(3):
+        assert torch.equal(p[i], p0[i])
+        assert torch.count_nonzero(m[i]) == 0
+        assert np.all(O[i] == 0)
+
+
+def test_deterministic_and_poisoned_workspace_agree():
+    p, g, m, _ = workloads.make_stack("d2", "cuda")
+    snap = [t.clone() for t in p + g + m]
+    run_gpu_step(p, g, m)
+    first = [t.clone() for t in p + m]
+    # same inputs again, with the bf16 workspace filled with NaN first
+    mu.muon_destroy()
+    mu.muon_init(debug_flags=mu.MUON_DEBUG_KEEP_O | mu.MUON_DEBUG_POISON_WORKSPACE, wait_timeout_s=2.0)
+    n = len(p)
+    for dst, src in zip(p + g + m, snap):
+        dst.copy_(src)
+    run_gpu_step(p, g, m)
+    for a, b in zip(first, p + m):
+        assert torch.equal(a, b)
+
+
+def test_multi_step_momentum_carried():
+    name = "d2"
+    p, g, m, shapes = workloads.make_stack(name, "cuda")
+    # the oracle carries its own weights and momentum from step to step
+    p_ref, m_ref = cpu_copy(p), cpu_copy(m)
+    for step in range(3):
+        if step > 0:
+            g = [workloads.make_grad(name, i, s, "cuda", 0, step) for i, s in enumerate(shapes)]
+        g0 = cpu_copy(g)
+        run_gpu_step(p, g, m, keep_o=False)
+        p1, m1 = cpu_copy(p), cpu_copy(m)
+        for i in range(len(p)):
+            p_ref[i], m_ref[i], _ = oracle.muon_matrix(p_ref[i], g0[i], m_ref[i], lr=np.float32(0.02),
+                                                       beta=np.float32(0.95), nesterov=True, ns_steps=5)
+            assert rel_fro(p1[i], p_ref[i]) <= 1e-3, (step, i)
+            assert rel_fro(m1[i], m_ref[i]) <= 1e-6, (step, i)
+
+
+def test_shape_list_changes_rebuild_the_plan():
+    for name in ("d2", "ragged", "d2"):
+        if name == "ragged":
+            p, g, m, _ = workloads.make_custom(RAGGED[:4], "cuda", tag="ragged")
+        else:
+            p, g, m, _ = workloads.make_stack(name, "cuda")
+        run_and_check(p, g, m, check_idx=[0, 1, 2, 3], tol_o=small_side_tol)
+
+
+def test_argument_errors_enqueue_nothing():
+    p, g, m, shapes = workloads.make_custom([(64, 64), (64, 128)], "cuda", tag="args")
+    before = [t.clone() for t in p + m]
+    # misaligned pointer (4 bytes into a buffer)
+    args = mu.StepArgs([p[0].data_ptr() + 4, p[1]], g, m, shapes=shapes)
+    assert mu.muon_step(args, check=False) == mu.MUON_ERR_MISALIGNED
+    assert mu.muon_step(p, g, m, shapes=[(64, 64), (64, 132)], check=False) == mu.MUON_ERR_UNSUPPORTED_SHAPE
+    assert mu.muon_step(p, g, m, ns_steps=6, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_step(p, g, m, ns_steps=-1, check=False) == mu.MUON_ERR_INVALID_ARG
+    args = mu.StepArgs([p[0], 0], g, m, shapes=shapes)
+    assert mu.muon_step(args, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_step([], [], [], check=False) == mu.MUON_OK
+    torch.cuda.synchronize()
+    for a, b in zip(before, p + m):
+        assert torch.equal(a, b)
+    assert mu.muon_get_status() == mu.MUON_OK
+
+
+def test_step_info_counts_launches():
+    p, g, m, shapes = workloads.make_stack("d2", "cuda")
+    run_gpu_step(p, g, m, keep_o=False)
+    info = mu.muon_get_step_info()
+    q = mu.muon_plan_query(shapes, 5)
+    assert info["launches"] == q["launches"] == 16
+    assert info["ns_alg_flops"] == q["ns_alg_flops"]
+
+
+@pytest.mark.slow
+def test_d26_full_stack_sampled():
+    # the full d26 stack in the configuration the benchmark times; the oracle
+    # checks the first and last layers' six matrices
+    p, g, m, _ = workloads.make_stack("d26", "cuda")
+    n = len(p)
+    run_and_check(p, g, m, check_idx=[0, 4, 5, n - 6, n - 2, n - 1])
