@@ -60,30 +60,77 @@ def load_peaks():
 
 
 class ClockSampler:
-    """Samples SM clocks and clock-event reasons through NVML every 100 ms."""
+    """Samples SM clocks, power and clock-event reasons during a timed region.
 
-    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+    Uses `nvidia-smi --query-gpu=... -lms 200` in a child process (the sampler
+    is started before the region and stopped after it); if nvidia-smi is not on
+    PATH, NVML through pynvml every 100 ms instead."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NVML_REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+                    "sw_power_cap": 0x4}
 
     def __init__(self, index: int):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self._stop = threading.Event()
+        self.index = index
+        self.samples, self.power, self.reasons, self.max_mhz = [], [], set(), None
+        self.source = None
+        self._proc = None
         self._nvml = None
+        self._stop = threading.Event()
+
+    # -- nvidia-smi
+    def _start_smi(self):
+        import shutil
+        import subprocess
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return False
+        self._proc = subprocess.Popen(
+            [exe, "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+             "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self.source = "nvidia-smi -lms 200"
+        return True
+
+    def _parse_smi(self, text):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in text.splitlines():
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                self.samples.append(float(parts[1]))
+                self.max_mhz = float(parts[2])
+                self.power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:]):
+                if val.lower() == "active":
+                    self.reasons.add(name)
+
+    # -- NVML fallback
+    def _start_nvml(self):
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # no NVML: the line says so
+        except Exception:
             self._nvml = None
+            return False
+        self.source = "nvml 100 ms"
+        self._t = threading.Thread(target=self._run_nvml, daemon=True)
+        self._t.start()
+        return True
 
-    def _run(self):
+    def _run_nvml(self):
         while not self._stop.is_set():
             try:
                 self.samples.append(self._nvml.nvmlDeviceGetClockInfo(self._h, self._nvml.NVML_CLOCK_SM))
                 mask = self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for name, bit in self.REASONS.items():
+                for name, bit in self.NVML_REASONS.items():
                     if mask & bit:
                         self.reasons.add(name)
             except Exception:
@@ -91,21 +138,29 @@ class ClockSampler:
             self._stop.wait(0.1)
 
     def __enter__(self):
-        if self._nvml is not None:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        if not self._start_smi():
+            self._start_nvml()
         return self
 
     def __exit__(self, *exc):
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
+            except Exception:
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            self._parse_smi(out or "")
         if self._nvml is not None:
             self._stop.set()
             self._t.join()
 
     def summary(self):
-        if self._nvml is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source (nvidia-smi, nvml)"]}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "power_w_max": max(self.power) if self.power else None, "source": self.source}
 
 
 # ---------------------------------------------------------------- CPU oracle leg
