@@ -62,7 +62,9 @@ typedef enum muon_status {
     MUON_ERR_OUT_OF_MEMORY = 6,       /* workspace allocation failed */
     MUON_ERR_DEVICE_TIMEOUT = 7,      /* a kernel's bounded wait expired (device status) */
     MUON_ERR_DEVICE_BOUNDS = 8,       /* a kernel saw an out-of-range tile (device status) */
-    MUON_ERR_UNSUPPORTED_DEVICE = 9   /* no device, or the current device is not sm_103 */
+    MUON_ERR_UNSUPPORTED_DEVICE = 9,  /* no device, or the current device is not sm_103 */
+    MUON_ERR_SCRATCH_LIMIT = 10       /* the request needs more than the fixed scratch of
+                                         muon_momentum_norm_noalloc holds */
 } muon_status;
 
 /* Stored (PyTorch (out_features, in_features)) shape of one parameter matrix. */
@@ -194,6 +196,56 @@ MUON_API muon_status muon_kernel_times(double* ms_out, int* launches_out, int n_
  */
 MUON_API muon_status muon_debug_copy_ns_output(int mat, float* dst_device, muon_stream_t stream);
 MUON_API muon_status muon_debug_copy_norms(float* dst_host, int n);
+
+/*
+ * Momentum + norm pass without any allocation.  (The pages have no counterpart:
+ * this entry point exists for callers, not for the method.)
+ *
+ * For callers that cannot call cudaMalloc.  Examples: a process whose device
+ * memory is already handed out by another runtime's caching pool, a service
+ * that must not allocate (cudaMalloc and cudaFree may synchronise the device
+ * and stall other streams) once it is serving, and code running where
+ * allocation is forbidden.  It runs the first stage of muon_step on the
+ * caller's buffers.  It allocates nothing, needs no muon_init, and keeps its
+ * scratch (per-tile norm partials, per-matrix tickets and constants) in one
+ * fixed array inside the library:
+ *
+ *   m' = beta m + g (stored back into momentum_bufs[i]); EMA form with
+ *        momentum_mode MUON_MOMENTUM_EMA, as in muon_step
+ *   u  = nesterov ? g + beta m' : m'
+ *   x0_out[i]  = bf16(u), round to nearest even, unscaled, in the oriented
+ *                layout: rows x cols row-major when rows <= cols, else the
+ *                transpose (cols x rows row-major)
+ *   norms_out[i] = ||u||_F (fp32, from a fixed-order fp64 sum of per-tile
+ *                  fp32 partials, so it is bitwise reproducible)
+ *
+ * Arguments: grads[i] (read only) and momentum_bufs[i] are device float32
+ * rows x cols; x0_out[i] is a device bf16 buffer of rows * cols elements;
+ * norms_out is a device float array of n_mats; all are caller-owned, and the
+ * matrix pointers must be 16-byte aligned (MUON_ERR_MISALIGNED).  Shapes follow
+ * the muon_step rule (MUON_ERR_UNSUPPORTED_SHAPE).  eps <= 0 selects 1e-7; it
+ * only enters an internal 1/(||u|| + eps) that this entry point does not return.
+ *
+ * Limits (MUON_ERR_SCRATCH_LIMIT beyond them, checked before anything is
+ * enqueued): n_mats <= 1024, and every group of 192 consecutive matrices
+ * covers at most 262144 tiles of 64 x 64 stored elements, i.e. at most about
+ * 1.07e9 elements.  The scratch array is about 1.02 MiB of device memory.
+ * Every device that loads the library holds it until the process exits.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current.  Make that first call before any stream capture begins.
+ * Later calls only enqueue work.  Every call on a device shares the one array:
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race and give wrong results.  Serialise them, e.g. on one stream.  Each call
+ * clears the tickets it uses before its kernel runs.
+ * Errors: MUON_ERR_INVALID_ARG, MUON_ERR_UNSUPPORTED_SHAPE, MUON_ERR_MISALIGNED,
+ * MUON_ERR_SCRATCH_LIMIT, MUON_ERR_UNSUPPORTED_DEVICE, MUON_ERR_CUDA.
+ */
+MUON_API muon_status muon_momentum_norm_noalloc(const float* const grads[], float* const momentum_bufs[],
+                                                void* const x0_out[], float* norms_out,
+                                                const muon_shape shapes[], int n_mats, float beta,
+                                                int nesterov, int momentum_mode, double eps,
+                                                muon_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,7 @@ MUON_ERR_OUT_OF_MEMORY = 6
 MUON_ERR_DEVICE_TIMEOUT = 7
 MUON_ERR_DEVICE_BOUNDS = 8
 MUON_ERR_UNSUPPORTED_DEVICE = 9
+MUON_ERR_SCRATCH_LIMIT = 10
 
 MUON_MOMENTUM_SGD_NESTEROV = 0
 MUON_MOMENTUM_EMA = 1
@@ -102,9 +103,12 @@ def lib():
         L.muon_debug_copy_norms.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         L.muon_plan_query.argtypes = [ctypes.POINTER(muon_shape), ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(muon_plan_info)]
+        L.muon_momentum_norm_noalloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                 vp, ctypes.POINTER(muon_shape), ctypes.c_int, ctypes.c_float,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_double, vp]
         for name in ("muon_init", "muon_step", "muon_destroy", "muon_get_status", "muon_get_step_info",
                      "muon_kernel_times", "muon_debug_copy_ns_output", "muon_debug_copy_norms",
-                     "muon_plan_query"):
+                     "muon_plan_query", "muon_momentum_norm_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -223,6 +227,31 @@ def muon_debug_copy_norms(n: int):
     buf = (ctypes.c_float * max(n, 1))()
     _check(lib().muon_debug_copy_norms(buf, int(n)), "muon_debug_copy_norms")
     return [buf[i] for i in range(n)]
+
+
+def muon_momentum_norm_noalloc(grads, momentum_bufs, x0_out, norms_out, beta: float = 0.95,
+                               nesterov: bool = True, momentum_mode: int = MUON_MOMENTUM_SGD_NESTEROV,
+                               eps: float = 0.0, stream=None, shapes=None, check: bool = True) -> int:
+    """The momentum + norm pass with no allocation (see include/muon.h).
+
+    For callers that may not allocate device memory: momentum_bufs are updated
+    in place, x0_out[i] (bf16 buffers of rows * cols elements) receive the
+    unscaled direction in the oriented layout, norms_out (float32, n) its
+    Frobenius norm.  Scratch lives in a fixed array inside the library."""
+    n = len(grads)
+    if len(momentum_bufs) != n or len(x0_out) != n:
+        raise ValueError("grads, momentum_bufs and x0_out must have the same length")
+    if shapes is None:
+        shapes = [tuple(g.shape) for g in grads]
+    vp = ctypes.c_void_p
+    g_arr = (vp * max(n, 1))(*[_ptr(x) for x in grads])
+    m_arr = (vp * max(n, 1))(*[_ptr(x) for x in momentum_bufs])
+    x_arr = (vp * max(n, 1))(*[_ptr(x) for x in x0_out])
+    s_arr = (muon_shape * max(n, 1))(*[muon_shape(int(r), int(c)) for r, c in shapes])
+    st = lib().muon_momentum_norm_noalloc(g_arr, m_arr, x_arr, _ptr(norms_out) if norms_out is not None else None,
+                                          s_arr, n, float(beta), 1 if nesterov else 0, int(momentum_mode),
+                                          float(eps), _stream(stream))
+    return _check(st, "muon_momentum_norm_noalloc") if check else st
 
 
 def declared_symbols() -> list:

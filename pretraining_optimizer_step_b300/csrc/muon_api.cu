@@ -355,6 +355,7 @@ const char* muon_status_string(muon_status s) {
         case MUON_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
         case MUON_ERR_DEVICE_BOUNDS: return "a kernel saw an out-of-range tile";
         case MUON_ERR_UNSUPPORTED_DEVICE: return "no sm_103 CUDA device";
+        case MUON_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of muon_momentum_norm_noalloc";
     }
     return "unknown status";
 }

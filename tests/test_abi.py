@@ -33,7 +33,7 @@ def test_library_hides_internal_symbols():
 
 
 def test_status_strings(L):
-    for code in range(0, 10):
+    for code in range(0, 11):
         s = mu.muon_status_string(code)
         assert s and s != "unknown status"
     assert mu.muon_status_string(1234) == "unknown status"
@@ -144,3 +144,33 @@ def test_plan_query_ns0_and_class_limit(L):
     shapes = [(8 * (k + 1), 64) for k in range(9)]
     q = mu.muon_plan_query(shapes, ns_steps=2)
     assert q["n_classes"] == 9 and q["launches"] == 1 + 3 * 2 * 2
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="passes fake pointers; host-side checks only")
+def test_noalloc_limits_are_checked_before_the_device(L):
+    # fake, 16-byte-aligned pointers: every case below must be rejected on the
+    # host, before any device work (there is no device here)
+    fake = 1 << 20
+    norms = 1 << 21
+    n = 1025  # more matrices than the fixed scratch has tickets for (1024)
+    st = mu.muon_momentum_norm_noalloc([fake] * n, [fake] * n, [fake] * n, norms, shapes=[(64, 64)] * n,
+                                       check=False)
+    assert st == mu.MUON_ERR_SCRATCH_LIMIT
+    # 17 matrices of 1024 x 16 tiles of 64 x 64 = 278528 tiles in one launch group (> 262144)
+    st = mu.muon_momentum_norm_noalloc([fake] * 17, [fake] * 17, [fake] * 17, norms,
+                                       shapes=[(65536, 1024)] * 17, check=False)
+    assert st == mu.MUON_ERR_SCRATCH_LIMIT
+    assert mu.muon_status_string(mu.MUON_ERR_SCRATCH_LIMIT).startswith("request exceeds")
+    # argument errors
+    assert mu.muon_momentum_norm_noalloc([fake], [fake], [fake], norms, shapes=[(64, 60)],
+                                         check=False) == mu.MUON_ERR_UNSUPPORTED_SHAPE
+    assert mu.muon_momentum_norm_noalloc([fake], [fake], [fake], norms, shapes=[(64, 64)], momentum_mode=3,
+                                         check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_momentum_norm_noalloc([fake + 4], [fake], [fake], norms, shapes=[(64, 64)],
+                                         check=False) == mu.MUON_ERR_MISALIGNED
+    assert mu.muon_momentum_norm_noalloc([fake], [fake], [0], norms, shapes=[(64, 64)],
+                                         check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_momentum_norm_noalloc([], [], [], norms, shapes=[], check=False) == mu.MUON_OK
+    # within the limits the call reaches the device check (none here)
+    assert mu.muon_momentum_norm_noalloc([fake], [fake], [fake], norms, shapes=[(64, 64)],
+                                         check=False) == mu.MUON_ERR_UNSUPPORTED_DEVICE
