@@ -90,6 +90,12 @@ class ClockSampler:
         self._proc = subprocess.Popen(
             [exe, "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
              "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        # wait (up to 5 s) for the sampler's first line, so that it is live when
+        # the timed region starts; that line was taken before the region and is dropped
+        import select
+        ready, _, _ = select.select([self._proc.stdout], [], [], 5.0)
+        if ready:
+            self._proc.stdout.readline()
         self.source = "nvidia-smi -lms 200"
         return True
 
@@ -161,6 +167,23 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples),
                 "power_w_max": max(self.power) if self.power else None, "source": self.source}
+
+
+# ---------------------------------------------------------------- multi-rank host logic
+def max_over_ranks(ms: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time: every rank times its own replica, the job's time is the max."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs one step of its own stack in ms_per_step (the max
+    over ranks), so the job does world x flops_per_rank_step in that time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -263,12 +286,7 @@ def run_ours(args, rank, world, local_rank):
         ev1.record(stream)
         ev1.synchronize()
         barrier()
-        ms = ev0.elapsed_time(ev1)
-        if dist is not None:
-            t = torch.tensor([ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
 
     # ---- timed region 1: plain steps (the headline value)
     mu.muon_init()
@@ -281,7 +299,7 @@ def run_ours(args, rank, world, local_rank):
     info = mu.muon_get_step_info()
     ms_step = total_ms / args.steps
     flops_step = info["ns_alg_flops"]
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, ms_step)
 
     # ---- timed region 2: same steps with CUDA events around every launch
     mu.muon_destroy()
@@ -353,7 +371,7 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
         ms_e2e = timed(e2e_steps, e2e_step) / e2e_steps
         mu.muon_get_status(stream)
-        e2e = {"value": world * flops_step / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
+        e2e = {"value": job_tflops(world, flops_step, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "path": "pinned host grads -> muon_step (C ABI) -> pinned host params, one stream"}
     mu.muon_destroy()

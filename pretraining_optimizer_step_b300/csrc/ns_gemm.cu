@@ -24,8 +24,10 @@
 //               128-byte swizzled, completion by mbarrier transaction bytes
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma 128x256x16,
 //               accumulators double-buffered in TMEM (2 x 256 fp32 columns)
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per warp, one output
-//               row per thread
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per warp into
+//               registers, staged through a per-warp 32 x 33 fp32 shared block so
+//               that global loads and stores run along rows (mirrored tiles and
+//               n x m weights read the block transposed)
 // Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, stops all
 // roles, drains its own TMA loads and MMAs, frees TMEM and returns.
 #include "kernels.cuh"
@@ -81,42 +83,17 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Writes 32 fp32 values (one thread's slice of a tile row) as bf16 to row `r`,
-// columns [c0, c0+32) of a row-major matrix with `ld` columns, in 16-byte
-// groups; columns >= limit are skipped (limit is a multiple of 8).
-__device__ __forceinline__ void store_row32(__nv_bfloat16* base, size_t ld, int r, int c0, int limit,
-                                            const float (&v)[32]) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const int c = c0 + 8 * g;
-        if (c < limit) {
-            uint4 w;
-            w.x = pack2(v[8 * g + 0], v[8 * g + 1]);
-            w.y = pack2(v[8 * g + 2], v[8 * g + 3]);
-            w.z = pack2(v[8 * g + 4], v[8 * g + 5]);
-            w.w = pack2(v[8 * g + 6], v[8 * g + 7]);
-            *reinterpret_cast<uint4*>(base + static_cast<size_t>(r) * ld + c) = w;
-        }
-    }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Reads 32 bf16 of row r, columns [c0, c0+32), as fp32 (zeros past limit).
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* base, size_t ld, int r, int c0,
-                                           int limit, float (&v)[32]) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const int c = c0 + 8 * g;
-        if (c < limit) {
-            const uint4 w = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(r) * ld + c);
-            v[8 * g + 0] = bf16_lo(w.x); v[8 * g + 1] = bf16_hi(w.x);
-            v[8 * g + 2] = bf16_lo(w.y); v[8 * g + 3] = bf16_hi(w.y);
-            v[8 * g + 4] = bf16_lo(w.z); v[8 * g + 5] = bf16_hi(w.z);
-            v[8 * g + 6] = bf16_lo(w.w); v[8 * g + 7] = bf16_hi(w.w);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[8 * g + j] = 0.f;
-        }
-    }
+// Four consecutive bf16 <-> fp32 at element offset `off` (a multiple of 4, so
+// the access is one aligned 8-byte word).
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* base, size_t off, const float (&v)[4]) {
+    uint2 w;
+    w.x = pack2(v[0], v[1]);
+    w.y = pack2(v[2], v[3]);
+    *reinterpret_cast<uint2*>(base + off) = w;
 }
 
 }  // namespace
@@ -130,6 +107,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_base_slot;
     __shared__ volatile int abort_flag;
+    __shared__ float stage_all[4][32][33];   // epilogue: one 32 x 32 fp32 block per warp (padded)
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t tiles_base = (raw + 1023u) & ~1023u;   // 128B-swizzle atoms need 1 KiB alignment
@@ -284,12 +262,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
         const int lg = warp & 3;               // TMEM lane group this warp may access
-        const int row_in_tile = lg * 32 + lane;
+        float (*stage)[33] = stage_all[lg];
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
             const TileCoord tc = decode_tile(P, t);
             const GemmClass& C = P.cls[tc.ci];
+            const int gm = C.mat_base + tc.mat;
+            const size_t mm = static_cast<size_t>(C.m) * C.m;
+            const size_t mn = static_cast<size_t>(C.m) * C.n;
+            const int r0 = tc.rb * kBM + lg * 32;        // first oriented row of this warp
+            const int ctile = sym ? tc.cb * kBM : tc.cb * kBN;
+            const int climit = sym ? C.m : C.n;
+            // While this tile's MMAs run, pull the global data its epilogue will read
+            // (the A or X tile, and the fp32 weights of the final launch) into L2,
+            // so that the epilogue's loads do not wait on DRAM.
+            if (P.mode != MODE_GRAM && r0 < C.m) {
+                const __nv_bfloat16* aux = C.aux + (sym ? static_cast<size_t>(tc.mat) * mm
+                                                        : static_cast<size_t>(tc.mat) * mn);
+                const int ld = sym ? C.m : C.n;
+                const int ncols = min(kBN, climit - ctile);          // multiple of 8
+                const int lines = (ncols * 2 + 127) / 128;           // 128-byte lines per row
+#pragma unroll 1
+                for (int q = lane; q < 32 * lines; q += 32) {
+                    const int rr = r0 + q / lines;
+                    if (rr < C.m)
+                        prefetch_l2(aux + static_cast<size_t>(rr) * ld + ctile + (q % lines) * 64);
+                }
+                if (P.mode == MODE_AXPY_FINAL) {
+                    const float* p = P.p_table[gm];
+                    if (!C.transposed) {
+                        const int plines = (ncols * 4 + 127) / 128;
+#pragma unroll 1
+                        for (int q = lane; q < 32 * plines; q += 32) {
+                            const int rr = r0 + q / plines;
+                            if (rr < C.m)
+                                prefetch_l2(p + static_cast<size_t>(rr) * C.n + ctile + (q % plines) * 32);
+                        }
+                    } else {
+                        // stored rows ctile .. ctile + ncols, columns r0 .. r0 + 31 (one line each)
+#pragma unroll 1
+                        for (int q = lane; q < ncols; q += 32)
+                            prefetch_l2(p + static_cast<size_t>(ctile + q) * C.m + r0);
+                    }
+                }
+            }
             // every lane waits; the outcome is made warp-uniform so that the
             // warp-collective TMEM loads below are reached by all lanes or none
             const bool ready = __all_sync(0xffffffffu,
@@ -300,89 +317,136 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
-            const int gm = C.mat_base + tc.mat;
-            const int r = tc.rb * kBM + row_in_tile;
-            const bool row_ok = r < C.m;
             const float s = P.first_iter ? P.inv_norm[gm] : 1.0f;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) +
                                    static_cast<uint32_t>(acc * kBN);
-            const size_t mm = static_cast<size_t>(C.m) * C.m;
-            const size_t mn = static_cast<size_t>(C.m) * C.n;
+            // Each chunk is a 32 x 32 fp32 block: TMEM rows are lanes, so the block is
+            // staged in shared memory and then read back by row segments (8 lanes x 4
+            // columns per row, 4 rows per instruction), so every global access of the
+            // epilogue is a run of >= 64 contiguous bytes.  A second pass over the
+            // stage reads it transposed for the mirrored tile and for weights stored
+            // n x m.  Each pass issues all of its global loads before using any.
+            const int seg_row = lane >> 3;               // 0..3
+            const int seg_col = (lane & 7) * 4;          // 0..28
+            float* p = nullptr;
+            float* dbg = nullptr;
+            float sc = 0.f;
+            if (P.mode == MODE_AXPY_FINAL) {
+                p = P.p_table[gm];
+                dbg = P.dbg_O ? P.dbg_O[gm] : nullptr;
+                sc = P.lr * P.aspect[gm];
+            }
+            const __nv_bfloat16* aux = nullptr;
+            __nv_bfloat16* out = nullptr;
+            if (sym) {
+                aux = P.mode == MODE_POLY ? C.aux + static_cast<size_t>(tc.mat) * mm : nullptr;
+                out = C.out + static_cast<size_t>(tc.mat) * mm;
+            } else {
+                aux = C.aux + static_cast<size_t>(tc.mat) * mn;
+                out = P.mode == MODE_AXPY ? C.out + static_cast<size_t>(tc.mat) * mn : nullptr;
+            }
+            const int ld = sym ? C.m : C.n;
+            const bool final_t = (P.mode == MODE_AXPY_FINAL) && C.transposed;
+            const bool final_n = (P.mode == MODE_AXPY_FINAL) && !C.transposed;
             for (int ch = 0; ch < kBN / 32; ++ch) {
                 uint32_t raw_v[32];
                 __syncwarp();
                 tmem_ld_32x32b_x32(t_row + ch * 32, raw_v);
-                tmem_ld_wait();
-                float v[32];
+                const int c0 = ctile + ch * 32;
+                const bool live = c0 < climit;  // warp-uniform
+                // issue this chunk's global loads while the TMEM load is in flight
+                uint2 araw[8];
+                float4 praw[8];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw_v[j]);
-                if (!row_ok) continue;
-                if (sym) {
-                    const int c0 = tc.cb * kBM + ch * 32;
-                    if (c0 >= C.m) continue;
-                    __nv_bfloat16* out = C.out + static_cast<size_t>(tc.mat) * mm;
+                for (int it = 0; it < 8; ++it) {
+                    const int grow = r0 + it * 4 + seg_row;
+                    const int gcol = c0 + seg_col;
+                    araw[it] = make_uint2(0u, 0u);
+                    praw[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (live && grow < C.m && gcol < climit) {
+                        const size_t off = static_cast<size_t>(grow) * ld + gcol;
+                        if (aux) araw[it] = *reinterpret_cast<const uint2*>(aux + off);
+                        if (final_n) praw[it] = *reinterpret_cast<const float4*>(p + off);
+                    }
+                    if (final_t) {
+                        // weights stored n x m: the pass-2 layout (stored row c0 + jj, columns r0 + rq ..)
+                        const int jj = it * 4 + seg_row;
+                        if (live && c0 + jj < climit && r0 + seg_col < C.m)
+                            praw[it] = *reinterpret_cast<const float4*>(p + static_cast<size_t>(c0 + jj) * C.m + r0 +
+                                                                        seg_col);
+                    }
+                }
+                tmem_ld_wait();
+                if (!live) continue;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) stage[lane][j] = __uint_as_float(raw_v[j]);
+                __syncwarp();
+                const bool mirror = sym && c0 >= (tc.rb + 1) * kBM;
+                // ---- pass 1: row segments of the oriented tile
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int i = it * 4 + seg_row;
+                    const int grow = r0 + i;
+                    const int gcol = c0 + seg_col;
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = stage[i][seg_col + e];
+                    if (grow >= C.m || gcol >= climit) continue;
+                    const size_t off = static_cast<size_t>(grow) * ld + gcol;
+                    const float a[4] = {bf16_lo(araw[it].x), bf16_hi(araw[it].x), bf16_lo(araw[it].y),
+                                        bf16_hi(araw[it].y)};
                     if (P.mode == MODE_GRAM) {
                         const float s2 = s * s;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= s2;
+                        for (int e = 0; e < 4; ++e) o[e] *= s2;
+                        store_bf16x4(out, off, o);
+                    } else if (P.mode == MODE_POLY) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[e] = fmaf(P.cc, o[e], P.cb * a[e]);
+                        store_bf16x4(out, off, o);
                     } else {
-                        float a[32];
-                        load_row32(C.aux + static_cast<size_t>(tc.mat) * mm, C.m, r, c0, C.m, a);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = fmaf(P.cc, v[j], P.cb * a[j]);
-                    }
-                    store_row32(out, C.m, r, c0, C.m, v);
-                    if (c0 >= (tc.rb + 1) * kBM) {
-                        // strictly above the diagonal block: also write the mirrored element
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (c0 + j < C.m)
-                                out[static_cast<size_t>(c0 + j) * C.m + r] = __float2bfloat16_rn(v[j]);
-                    }
-                } else {
-                    const int c0 = tc.cb * kBN + ch * 32;
-                    if (c0 >= C.n) continue;
-                    float x[32];
-                    load_row32(C.aux + static_cast<size_t>(tc.mat) * mn, C.n, r, c0, C.n, x);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = s * fmaf(P.ca, x[j], v[j]);
-                    if (P.mode == MODE_AXPY) {
-                        store_row32(C.out + static_cast<size_t>(tc.mat) * mn, C.n, r, c0, C.n, v);
-                    } else {
-                        float* p = P.p_table[gm];
-                        float* dbg = P.dbg_O ? P.dbg_O[gm] : nullptr;
-                        const float sc = P.lr * P.aspect[gm];
-                        if (!C.transposed) {
-                            // stored layout = oriented layout (m x n)
-#pragma unroll
-                            for (int g = 0; g < 8; ++g) {
-                                const int c = c0 + 4 * g;
-                                if (c < C.n) {
-                                    float4* pp = reinterpret_cast<float4*>(p + static_cast<size_t>(r) * C.n + c);
-                                    float4 w = *pp;
-                                    w.x = fmaf(-sc, v[4 * g + 0], w.x);
-                                    w.y = fmaf(-sc, v[4 * g + 1], w.y);
-                                    w.z = fmaf(-sc, v[4 * g + 2], w.z);
-                                    w.w = fmaf(-sc, v[4 * g + 3], w.w);
-                                    *pp = w;
-                                    if (dbg)
-                                        *reinterpret_cast<float4*>(dbg + static_cast<size_t>(r) * C.n + c) =
-                                            make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-                                }
-                            }
-                        } else {
-                            // stored matrix is n x m: O_stored[c][r] = O[r][c]; consecutive
-                            // lanes hold consecutive r, so each column c is a coalesced row segment
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int c = c0 + j;
-                                if (c < C.n) {
-                                    const size_t po = static_cast<size_t>(c) * C.m + r;
-                                    p[po] = fmaf(-sc, v[j], p[po]);
-                                    if (dbg) dbg[po] = v[j];
-                                }
-                            }
+                        for (int e = 0; e < 4; ++e) o[e] = s * fmaf(P.ca, a[e], o[e]);
+                        if (P.mode == MODE_AXPY) {
+                            store_bf16x4(out, off, o);
+                        } else if (final_n) {
+                            float4 w = praw[it];
+                            w.x = fmaf(-sc, o[0], w.x);
+                            w.y = fmaf(-sc, o[1], w.y);
+                            w.z = fmaf(-sc, o[2], w.z);
+                            w.w = fmaf(-sc, o[3], w.w);
+                            *reinterpret_cast<float4*>(p + off) = w;
+                            if (dbg) *reinterpret_cast<float4*>(dbg + off) = make_float4(o[0], o[1], o[2], o[3]);
                         }
+                    }
+                    if (mirror || final_t) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) stage[i][seg_col + e] = o[e];
+                    }
+                }
+                if (!(mirror || final_t)) continue;  // warp-uniform
+                __syncwarp();
+                // ---- pass 2: the transposed block (stored row c0 + jj, columns r0 + rq ..)
+                const int rq = seg_col;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int jj = it * 4 + seg_row;
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = stage[rq + e][jj];
+                    if (c0 + jj >= climit || r0 + rq >= C.m) continue;
+                    const size_t off = static_cast<size_t>(c0 + jj) * C.m + r0 + rq;
+                    if (mirror) {
+                        store_bf16x4(out, off, o);
+                    } else {
+                        // weights stored n x m: O_stored[c][r] = O[r][c]
+                        float4 w = praw[it];
+                        w.x = fmaf(-sc, o[0], w.x);
+                        w.y = fmaf(-sc, o[1], w.y);
+                        w.z = fmaf(-sc, o[2], w.z);
+                        w.w = fmaf(-sc, o[3], w.w);
+                        *reinterpret_cast<float4*>(p + off) = w;
+                        if (dbg) *reinterpret_cast<float4*>(dbg + off) = make_float4(o[0], o[1], o[2], o[3]);
                     }
                 }
             }
