@@ -82,9 +82,11 @@ enum {
     MUON_DEBUG_KEEP_O = 1,            /* also write O (fp32, stored layout) for muon_debug_copy_ns_output */
     MUON_DEBUG_POISON_WORKSPACE = 2,  /* fill the bf16 workspace with NaN before every step */
     MUON_DEBUG_TIME_KERNELS = 4,      /* record CUDA events around every launch (muon_kernel_times) */
-    MUON_DEBUG_INJECT_LOST_LOAD = 8   /* test hook: one operand load of the first Gram launch is never
+    MUON_DEBUG_INJECT_LOST_LOAD = 8,  /* test hook: one operand load of the first Gram launch is never
                                          issued, so the consumer's bounded wait must expire and the step
                                          reports MUON_ERR_DEVICE_TIMEOUT; the result is then invalid */
+    MUON_DEBUG_SINGLE_CTA_GEMM = 16   /* ablation: run the Newton-Schulz GEMMs as 128 x 256 single-CTA
+                                         tiles instead of 256 x 256 CTA-pair tiles (same results) */
 };
 
 typedef struct muon_config {

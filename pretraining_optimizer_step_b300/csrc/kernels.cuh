@@ -118,4 +118,55 @@ cudaError_t launch_update(const UpdateParams& p, cudaStream_t s);
 cudaError_t launch_ns_gemm(const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t ns_gemm_prepare();  // one-time kernel attribute setup
 
+// ------------------------------------------------------------------ Newton-Schulz GEMM on CTA pairs
+// A cluster of two CTAs computes a 256 x N tile (N = 256, or 128 for a ragged
+// last column tile) with tcgen05.mma.cta_group::2: each CTA holds 128 rows of
+// the A operand and N/2 rows of the B operand per pipeline stage, and receives
+// its 128 rows of the accumulator in its own TMEM.
+constexpr int kPairStages = 4;
+constexpr int kPairAStageBytes = 128 * 64 * 2;               // 16 KiB: 128 rows x 64 K of bf16
+constexpr int kPairBStageBytes = 128 * 64 * 2;               // 16 KiB: up to 128 B-side rows (N/2)
+constexpr int kPairStageBytes = kPairAStageBytes + kPairBStageBytes;
+constexpr int kEpiInSlotBytes = 6144;                        // fp32 32x32 (4 KiB) + bf16 32x32 (2 KiB)
+constexpr int kEpiOutSlotBytes = 4096;                       // bf16 32x32 direct + mirror, or fp32 32x32
+constexpr int kEpiWarpBytes = 2 * kEpiInSlotBytes + kEpiOutSlotBytes;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 4 * kEpiWarpBytes + 1024;
+
+struct PairClass {
+    int m, n;             // oriented X is m x n (m <= n)
+    int nmats;
+    int tile_begin;       // first pair tile of this class in the launch
+    int tiles_per_mat;    // pair tiles per matrix
+    int k_blocks;         // ceil(K / 64)
+    int row_blocks;       // ceil(m / 128)
+    int col_groups;       // Gram/poly: ceil(row_blocks / 2) column pairs; axpy: ceil(n / 256) column tiles
+    int transposed;       // stored matrix is n x m
+    int mat_base;         // step position of the class's first matrix
+};
+
+struct PairParams {
+    CUtensorMap tmA[kMaxClasses];    // A side, K-major, box 64 (K) x 128 rows, 128B swizzle
+    CUtensorMap tmB[kMaxClasses];    // B side: Gram/poly K-major box 64 x 64; axpy MN-major box 64 cols x 64 K
+    CUtensorMap tmIn[kMaxClasses];   // epilogue input (poly: A, axpy: X), bf16 box 32 x 32, 64B swizzle
+    CUtensorMap tmOut[kMaxClasses];  // epilogue output (gram: A, poly: B, axpy: X'), bf16 box 32 x 32, 64B swizzle
+    PairClass cls[kMaxClasses];
+    int nclasses;
+    int total_tiles;      // pair tiles
+    int mode;             // GemmMode
+    int first_iter;
+    float ca, cb, cc;
+    const float* inv_norm;
+    const float* aspect;
+    float lr;
+    const CUtensorMap* p_maps;    // per step position: fp32 weights (stored layout), box 32 x 32, 128B swizzle
+    const CUtensorMap* dbg_maps;  // per step position (O, stored layout) or nullptr
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int inject_lost_load;
+};
+
+cudaError_t launch_ns_pair(const PairParams& p, int clusters, cudaStream_t s);
+cudaError_t ns_pair_prepare(int* max_clusters);  // kernel attributes; co-resident clusters of two
+
+
 }  // namespace muon

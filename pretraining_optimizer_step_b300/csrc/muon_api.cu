@@ -32,7 +32,10 @@ struct ClassPlan {
     __nv_bfloat16* A = nullptr;
     __nv_bfloat16* B = nullptr;
     CUtensorMap tmXk[2], tmXmn[2], tmAk, tmBk;
+    // CTA-pair kernel: B-side K-major maps (box 64 x 64) and epilogue subtile maps (bf16 32 x 32)
+    CUtensorMap tmXk64[2], tmAk64, epiX[2], epiA, epiB;
     int row_blocks = 0, col_tiles = 0, sym_tiles = 0, axpy_tiles = 0;
+    int col_pairs = 0, sym_pair_tiles = 0, axpy_pair_tiles = 0;
 };
 
 struct Plan {
@@ -54,6 +57,9 @@ struct Plan {
     size_t workspace_bf16_bytes = 0;
     char* workspace_bf16 = nullptr;
     std::vector<float*> dbg_O;      // host copies of the O buffer pointers
+    CUtensorMap* p_maps = nullptr;  // device: fp32 weight maps per position (refreshed when params change)
+    CUtensorMap* dbg_maps = nullptr;  // device: O maps per position (KEEP_O)
+    std::vector<float*> mapped_p;   // params the device p_maps describe, by step index
     double ns_flops_per_iter = 0.0;
     double elem_bytes = 0.0;
 };
@@ -66,6 +72,7 @@ struct PendingTime {
 struct Context {
     int device = -1;
     int sm_count = 0;
+    int max_clusters = 0;           // co-resident CTA pairs of the pair kernel
     std::vector<double> coeffs;
     int n_rows = 0;
     double eps = 1e-7;
@@ -107,6 +114,50 @@ muon_status encode_map(EncodeTiledFn enc, CUtensorMap* map, void* base, int cols
     return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
 }
 
+muon_status encode_map_ex(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dtype, int esize, void* base,
+                          int cols, int rows, int depth, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
+    const cuuint32_t rank = depth > 0 ? 3 : 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(depth > 0 ? depth : 1)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esize,
+                             static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * esize};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype, rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
+}
+
+// fp32 weight (or O) matrix in its stored r x c layout, 32 x 32 boxes, 128B swizzle.
+muon_status encode_f32_map(EncodeTiledFn enc, CUtensorMap* map, float* base, int rows, int cols) {
+    return encode_map_ex(enc, map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, 0, 32, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// CTA-pair tiling: Gram/poly tiles per matrix (column pairs q, row pairs 0..q) and their
+// executed flops; axpy tiles per matrix (row pairs x 256-column tiles).
+int pair_col_pairs(int row_blocks) { return (row_blocks + 1) / 2; }
+int pair_sym_tiles(int row_blocks) {
+    const int Q = pair_col_pairs(row_blocks);
+    return Q * (Q + 1) / 2;
+}
+double pair_sym_exec_flops(int row_blocks, int K) {
+    double f = 0.0;
+    for (int q = 0; q < pair_col_pairs(row_blocks); ++q) {
+        const int ncols = (2 * q + 1 < row_blocks) ? 256 : 128;
+        f += static_cast<double>(q + 1) * 2.0 * 256.0 * ncols * K;
+    }
+    return f;
+}
+double pair_axpy_exec_flops(int row_blocks, int n, int K) {
+    double f = 0.0;
+    for (int c0 = 0; c0 < n; c0 += 256) {
+        const int ncols = (n - c0 > 128) ? 256 : 128;
+        f += static_cast<double>(pair_col_pairs(row_blocks)) * 2.0 * 256.0 * ncols * K;
+    }
+    return f;
+}
+
 int sym_tiles_per_mat(int row_blocks) {
     int t = 0;
     for (int bi = 0; bi < row_blocks; ++bi) t += (row_blocks - bi + 1) / 2;
@@ -116,6 +167,7 @@ int sym_tiles_per_mat(int row_blocks) {
 // Host-only part of planning: shape classes, arena layout, tile counts.
 struct Layout {
     std::vector<size_t> offX0, offX1, offA, offB, off_dbg;
+    size_t off_pmaps = 0, off_dmaps = 0;
     size_t bf16_end = 0, off_inv = 0, off_nrm = 0, off_asp = 0, off_cnt = 0, off_pt = 0, off_dt = 0,
            off_part = 0, total = 0;
     int momentum_ctas = 0;
@@ -167,12 +219,16 @@ void compute_layout(Plan* P, const muon_shape* shapes, int n, bool keep_o, Layou
         cp.col_tiles = (cp.n + kBN - 1) / kBN;
         cp.sym_tiles = sym_tiles_per_mat(cp.row_blocks);
         cp.axpy_tiles = cp.row_blocks * cp.col_tiles;
+        cp.col_pairs = pair_col_pairs(cp.row_blocks);
+        cp.sym_pair_tiles = pair_sym_tiles(cp.row_blocks);
+        cp.axpy_pair_tiles = cp.col_pairs * cp.col_tiles;
         const double m = cp.m, nn = cp.n;
         P->ns_flops_per_iter += static_cast<double>(G) * (3.0 * m * m * nn + m * m * m);
-        L->ns_exec_flops_per_iter += static_cast<double>(G) * 2.0 * kBM * kBN *
-            (static_cast<double>(cp.sym_tiles) * (cp.n + cp.m) + static_cast<double>(cp.axpy_tiles) * cp.m);
-        L->sym_tiles += static_cast<long long>(G) * cp.sym_tiles;
-        L->axpy_tiles += static_cast<long long>(G) * cp.axpy_tiles;
+        L->ns_exec_flops_per_iter += static_cast<double>(G) *
+            (pair_sym_exec_flops(cp.row_blocks, cp.n) + pair_sym_exec_flops(cp.row_blocks, cp.m) +
+             pair_axpy_exec_flops(cp.row_blocks, cp.n, cp.m));
+        L->sym_tiles += static_cast<long long>(G) * cp.sym_pair_tiles;
+        L->axpy_tiles += static_cast<long long>(G) * cp.axpy_pair_tiles;
         P->elem_bytes += static_cast<double>(G) * m * nn * 22.0;
     }
     L->bf16_end = off;
@@ -182,6 +238,8 @@ void compute_layout(Plan* P, const muon_shape* shapes, int n, bool keep_o, Layou
     L->off_cnt = off; off = align_up(off + n * sizeof(unsigned int), 256);
     L->off_pt = off; off = align_up(off + n * sizeof(float*), 256);
     L->off_dt = off; off = align_up(off + n * sizeof(float*), 256);
+    L->off_pmaps = off; off = align_up(off + n * sizeof(CUtensorMap), 256);
+    L->off_dmaps = off; off = align_up(off + n * sizeof(CUtensorMap), 256);
     // one partial per momentum CTA of the largest launch chunk
     size_t max_tiles = 0, chunk_tiles = 0;
     for (int k = 0; k < n; ++k) {
@@ -238,6 +296,20 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
         }
         if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmAk, cp.A, cp.m, cp.m, G, kBK, kBM);
         if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmBk, cp.B, cp.m, cp.m, G, kBK, kBM);
+        const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        for (int pp = 0; pp < 2 && st == MUON_OK; ++pp) {
+            st = encode_map_ex(ctx->encode, &cp.tmXk64[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, kBK, 64,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+            if (st == MUON_OK)
+                st = encode_map_ex(ctx->encode, &cp.epiX[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 32, 32,
+                                   CU_TENSOR_MAP_SWIZZLE_64B);
+        }
+        if (st == MUON_OK)
+            st = encode_map_ex(ctx->encode, &cp.tmAk64, bf, 2, cp.A, cp.m, cp.m, G, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st == MUON_OK)
+            st = encode_map_ex(ctx->encode, &cp.epiA, bf, 2, cp.A, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (st == MUON_OK)
+            st = encode_map_ex(ctx->encode, &cp.epiB, bf, 2, cp.B, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != MUON_OK) {
             free_plan(P);
             return st;
@@ -263,6 +335,23 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
     P->dbg_O.assign(n, nullptr);
     for (int i = 0; i < n; ++i)
         if (!L.off_dbg.empty()) P->dbg_O[i] = reinterpret_cast<float*>(a + L.off_dbg[i]);
+    P->p_maps = reinterpret_cast<CUtensorMap*>(a + L.off_pmaps);
+    P->mapped_p.assign(n, nullptr);
+    if (!L.off_dbg.empty()) {
+        P->dbg_maps = reinterpret_cast<CUtensorMap*>(a + L.off_dmaps);
+        std::vector<CUtensorMap> dm(n);
+        for (int k = 0; k < n; ++k) {
+            const int i = P->order[k];
+            if (encode_f32_map(ctx->encode, &dm[k], P->dbg_O[i], shapes[i].rows, shapes[i].cols) != MUON_OK) {
+                free_plan(P);
+                return MUON_ERR_CUDA;
+            }
+        }
+        if (cudaMemcpy(P->dbg_maps, dm.data(), n * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess) {
+            free_plan(P);
+            return MUON_ERR_CUDA;
+        }
+    }
     bool ok = cudaMemcpy(P->aspect, asp.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && cudaMemcpy(P->dbg_table, dbg.data(), n * sizeof(float*), cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && cudaMemset(P->counters, 0, n * sizeof(unsigned int)) == cudaSuccess;
@@ -428,7 +517,8 @@ muon_status muon_init(const muon_config* cfg) {
         return MUON_ERR_CUDA;
     }
     ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (ns_gemm_prepare() != cudaSuccess ||
+    if (ns_gemm_prepare() != cudaSuccess || ns_pair_prepare(&ctx->max_clusters) != cudaSuccess ||
+        ctx->max_clusters < 1 ||
         cudaMalloc(&ctx->status, sizeof(unsigned int)) != cudaSuccess ||
         cudaMemset(ctx->status, 0, sizeof(unsigned int)) != cudaSuccess) {
         cudaGetLastError();
@@ -534,8 +624,107 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
     }
 
     // ---- Newton-Schulz iterations: per group of <= kMaxClasses classes
-    static GemmParams gp;
     const int nclass = static_cast<int>(P->classes.size());
+    if (!(ctx->debug & MUON_DEBUG_SINGLE_CTA_GEMM)) {
+        // fp32 weight maps of the fused update: re-encoded only when the params change
+        bool changed = false;
+        for (int i = 0; i < n_mats && !changed; ++i) changed = P->mapped_p[i] != params[i];
+        if (changed) {
+            std::vector<CUtensorMap> pm(n_mats);
+            for (int k = 0; k < n_mats; ++k) {
+                const int i = P->order[k];
+                if (encode_f32_map(ctx->encode, &pm[k], params[i], shapes[i].rows, shapes[i].cols) != MUON_OK)
+                    return MUON_ERR_CUDA;
+            }
+            // launches already enqueued may still read the previous maps
+            if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+            if (cudaMemcpy(P->p_maps, pm.data(), n_mats * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
+                return MUON_ERR_CUDA;
+            P->mapped_p.assign(params, params + n_mats);
+        }
+        static PairParams pp;  // ~5 KiB: kept off the stack
+        for (int it = 0; it < ns_steps; ++it) {
+            const double* row = &ctx->coeffs[3 * it];
+            const int pin = it & 1, pout = pin ^ 1;
+            const bool last = (it == ns_steps - 1);
+            for (int g0 = 0; g0 < nclass; g0 += kMaxClasses) {
+                const int gc = std::min(kMaxClasses, nclass - g0);
+                for (int mode = MODE_GRAM; mode <= MODE_AXPY; ++mode) {
+                    std::memset(&pp, 0, sizeof(pp));
+                    const int eff_mode = (mode == MODE_AXPY && last) ? MODE_AXPY_FINAL : mode;
+                    pp.mode = eff_mode;
+                    pp.nclasses = gc;
+                    pp.first_iter = (it == 0 && mode != MODE_POLY) ? 1 : 0;
+                    pp.ca = static_cast<float>(row[0]);
+                    pp.cb = static_cast<float>(row[1]);
+                    pp.cc = static_cast<float>(row[2]);
+                    pp.inv_norm = P->inv_norm;
+                    pp.aspect = P->aspect;
+                    pp.lr = lr;
+                    pp.p_maps = P->p_maps;
+                    pp.dbg_maps = keep_o ? P->dbg_maps : nullptr;
+                    pp.status = ctx->status;
+                    pp.timeout_ns = ctx->timeout_ns;
+                    pp.inject_lost_load = ((ctx->debug & MUON_DEBUG_INJECT_LOST_LOAD) && !ctx->injected &&
+                                           it == 0 && mode == MODE_GRAM && g0 == 0)
+                                              ? 1
+                                              : 0;
+                    if (pp.inject_lost_load) ctx->injected = true;
+                    int tiles = 0;
+                    int mat_base = 0;
+                    for (int k = 0; k < g0; ++k) mat_base += static_cast<int>(P->classes[k].mats.size());
+                    for (int k = 0; k < gc; ++k) {
+                        const ClassPlan& cp = P->classes[g0 + k];
+                        PairClass& C = pp.cls[k];
+                        const int G = static_cast<int>(cp.mats.size());
+                        C.m = cp.m;
+                        C.n = cp.n;
+                        C.nmats = G;
+                        C.tile_begin = tiles;
+                        C.row_blocks = cp.row_blocks;
+                        C.transposed = cp.transposed;
+                        C.mat_base = mat_base;
+                        if (mode == MODE_GRAM) {
+                            C.tiles_per_mat = cp.sym_pair_tiles;
+                            C.col_groups = cp.col_pairs;
+                            C.k_blocks = (cp.n + kBK - 1) / kBK;
+                            pp.tmA[k] = cp.tmXk[pin];
+                            pp.tmB[k] = cp.tmXk64[pin];
+                            pp.tmIn[k] = cp.epiX[pin];
+                            pp.tmOut[k] = cp.epiA;
+                        } else if (mode == MODE_POLY) {
+                            C.tiles_per_mat = cp.sym_pair_tiles;
+                            C.col_groups = cp.col_pairs;
+                            C.k_blocks = (cp.m + kBK - 1) / kBK;
+                            pp.tmA[k] = cp.tmAk;
+                            pp.tmB[k] = cp.tmAk64;
+                            pp.tmIn[k] = cp.epiA;
+                            pp.tmOut[k] = cp.epiB;
+                        } else {
+                            C.tiles_per_mat = cp.axpy_pair_tiles;
+                            C.col_groups = cp.col_tiles;
+                            C.k_blocks = (cp.m + kBK - 1) / kBK;
+                            pp.tmA[k] = cp.tmBk;
+                            pp.tmB[k] = cp.tmXmn[pin];
+                            pp.tmIn[k] = cp.epiX[pin];
+                            pp.tmOut[k] = cp.epiX[pout];
+                        }
+                        tiles += C.tiles_per_mat * G;
+                        mat_base += G;
+                    }
+                    pp.total_tiles = tiles;
+                    const int clusters = std::min(tiles, ctx->max_clusters);
+                    const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3 : 4;
+                    const muon_status st =
+                        timed_launch(ctx, kind, stream, [&] { return launch_ns_pair(pp, clusters, stream); });
+                    if (st != MUON_OK) return st;
+                }
+            }
+        }
+        return MUON_OK;
+    }
+    // single-CTA kernel (MUON_DEBUG_SINGLE_CTA_GEMM): 128 x 256 tiles, one CTA per tile
+    static GemmParams gp;
     for (int it = 0; it < ns_steps; ++it) {
         const double* row = &ctx->coeffs[3 * it];
         const int pin = it & 1, pout = pin ^ 1;

@@ -1,0 +1,502 @@
+// ns_pair.cu -- the Newton-Schulz GEMMs of the Muon step on CTA pairs.
+//
+// One iteration of the quintic loop ("Cara Melatih ChatGPT Sendiri dengan
+// Budget 50 Dolar", section "2. Pengoptimal Muon", orthogonalization loop) is
+// three launches of this kernel over every matrix of the step (grouped by
+// oriented shape class); the modes and their epilogues are those of
+// ns_gemm.cu:
+//   MODE_GRAM        A = s^2 X X^T          tiles on/above the diagonal, mirrored on store
+//   MODE_POLY        B = b A + c A A        A symmetric: A A = A A^T, same operand both sides
+//   MODE_AXPY        X' = s (a X + B X)     X read MN-major as the B operand
+//   MODE_AXPY_FINAL  O = s (a X + B X) in fp32, p -= lr sqrt(max(1, r/c)) O
+//
+// A cluster of two CTAs (one per SM) computes a 256 x N tile with
+// tcgen05.mma.cta_group::2: CTA rank r holds rows [128 r, 128 r + 128) of the A
+// operand and half of the N rows of the B operand in its shared memory, and
+// receives its 128 accumulator rows in its own TMEM.  Per SM this halves the B
+// operand traffic against a 128 x 256 single-CTA tile.
+//   Gram/poly: tile = row blocks (2 rp, 2 rp + 1) x column blocks (2 q, 2 q + 1),
+//              rp <= q; N = 128 when column block 2 q + 1 does not exist.  The
+//              lower block of a diagonal tile is computed but not stored.
+//   axpy:      tile = row blocks (2 rp, 2 rp + 1) x columns [256 ct, 256 ct + N).
+//
+// CTA layout (192 threads, persistent over the pair tiles):
+//   warp 0      TMA producer (both CTAs): 4-stage ring of {A 128 x 64, B-half <= 128 x 64};
+//               the loads of both CTAs complete on the even CTA's mbarrier
+//   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues the MMAs
+//               (M 256, N 256/128, K 16) and commits to both CTAs' barriers
+//   warps 2..5  epilogue (both CTAs): per warp 32 rows, in chunks of 32 columns.
+//               Inputs (the A or X tile, the fp32 weights) arrive by TMA into two
+//               swizzled shared slots, one chunk ahead; outputs leave by TMA store
+//               from a swizzled shared slot.  Threads touch shared memory only
+//               with conflict-free 16-byte vectors (row access) or 4-byte/2-byte
+//               column access of 128-byte rows (transposes).
+// Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, raises its
+// abort flag, lets its own copies land, and joins the final cluster barrier.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace muon {
+
+namespace {
+
+struct PairTile {
+    int ci;      // class
+    int mat;     // matrix within the class
+    int rb;      // this CTA's row block (128 rows)
+    int c0;      // first output column of the tile
+    int ncols;   // N: 256 or 128
+};
+
+__device__ __forceinline__ PairTile decode_pair_tile(const PairParams& P, int t, int rank, bool sym) {
+    PairTile pt;
+    int ci = 0;
+    while (ci + 1 < P.nclasses && t >= P.cls[ci + 1].tile_begin) ++ci;
+    const PairClass& C = P.cls[ci];
+    const int local = t - C.tile_begin;
+    pt.ci = ci;
+    pt.mat = local / C.tiles_per_mat;
+    const int lt = local - pt.mat * C.tiles_per_mat;
+    if (sym) {
+        // column pair q has q + 1 tiles (row pairs 0..q)
+        int q = 0, base = 0;
+        while (base + q + 1 <= lt) {
+            base += q + 1;
+            ++q;
+        }
+        const int rp = lt - base;
+        pt.rb = 2 * rp + rank;
+        pt.c0 = 256 * q;
+        pt.ncols = (2 * q + 1 < C.row_blocks) ? 256 : 128;
+    } else {
+        const int rp = lt / C.col_groups;
+        const int ct = lt - rp * C.col_groups;
+        pt.rb = 2 * rp + rank;
+        pt.c0 = 256 * ct;
+        pt.ncols = (C.n - pt.c0 > 128) ? 256 : 128;
+    }
+    return pt;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Byte offsets inside the swizzled 32 x 32 subtiles the epilogue TMA maps use.
+// bf16, 64-byte rows, 64B swizzle: 16-byte unit u of row r lives at unit u ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint32_t sw64_unit(int r, int u) { return r * 64 + ((u ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_unit(r, c >> 3) + ((c & 7) << 1); }
+// fp32, 128-byte rows, 128B swizzle: 16-byte unit u of row r lives at unit u ^ (r & 7).
+__device__ __forceinline__ uint32_t sw128_unit(int r, int u) { return r * 128 + ((u ^ (r & 7)) << 4); }
+__device__ __forceinline__ uint32_t sw128_elem(int r, int c) { return sw128_unit(r, c >> 2) + ((c & 3) << 2); }
+
+__device__ __forceinline__ void latch_status(unsigned int* status, unsigned int bits) { atomicOr(status, bits); }
+
+// Bounded spin on the global timer (lets copies still in flight land before
+// an aborting CTA leaves).
+__device__ __forceinline__ void settle_ns(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) {
+    }
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    ns_pair_kernel(const __grid_constant__ PairParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kPairStages];
+    __shared__ __align__(8) uint64_t empty_bar[kPairStages];
+    __shared__ __align__(8) uint64_t tfull_bar[2];
+    __shared__ __align__(8) uint64_t tempty_bar[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ __align__(8) uint64_t in_bar[4][2];
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ volatile int abort_flag;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t tiles_base = (raw + 1023u) & ~1023u;
+    uint8_t* tiles_ptr = smem_raw + (tiles_base - raw);
+    uint8_t* epi_ptr = tiles_ptr + kPairStages * kPairStageBytes;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool leader = rank == 0;
+    const int cluster = static_cast<int>(cluster_id_x());
+    const int nclusters = static_cast<int>(cluster_count_x());
+    const bool sym = (P.mode == MODE_GRAM || P.mode == MODE_POLY);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull_bar[a], 1);
+            mbar_init(&tempty_bar[a], 8);  // one arrive per epilogue warp of both CTAs
+        }
+        mbar_init(&drain_bar, 1);
+        for (int w = 0; w < 4; ++w) {
+            mbar_init(&in_bar[w][0], 1);
+            mbar_init(&in_bar[w][1], 1);
+        }
+        abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&tmem_base_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        for (int c = 0; c < P.nclasses; ++c) {
+            tma_prefetch_desc(&P.tmA[c]);
+            tma_prefetch_desc(&P.tmB[c]);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        bool aborted = false;
+        bool injected = false;
+        for (int t = cluster; t < P.total_tiles && !aborted; t += nclusters) {
+            const PairTile pt = decode_pair_tile(P, t, rank, sym);
+            const PairClass& C = P.cls[pt.ci];
+            const CUtensorMap* mA = &P.tmA[pt.ci];
+            const CUtensorMap* mB = &P.tmB[pt.ci];
+            const int half = pt.ncols >> 1;             // this CTA's B-side rows/columns: 64 or 128
+            const int b0 = pt.c0 + rank * half;         // first of them
+            const uint32_t total_bytes = 2u * (kPairAStageBytes + static_cast<uint32_t>(half) * kBK * 2u);
+            for (int kb = 0; kb < C.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, P.timeout_ns)) {
+                    latch_status(P.status, STATUS_TIMEOUT);
+                    abort_flag = 1;
+                    aborted = true;
+                    break;
+                }
+                uint8_t* sa = tiles_ptr + stage * kPairStageBytes;
+                uint8_t* sb = sa + kPairAStageBytes;
+                const int k0 = kb * kBK;
+                const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                if (leader) mbar_arrive_expect_tx(&full_bar[stage], total_bytes);
+                if (P.inject_lost_load && leader && !injected && cluster == 0) {
+                    injected = true;  // test hook: this A slice never arrives
+                } else {
+                    tma_load_3d_pair(sa, mA, bar, k0, pt.rb * 128, pt.mat);
+                }
+                for (int j = 0; j < half / 64; ++j) {
+                    if (sym)
+                        tma_load_3d_pair(sb + j * (64 * 128), mB, bar, k0, b0 + 64 * j, pt.mat);
+                    else
+                        tma_load_3d_pair(sb + j * (64 * 128), mB, bar, b0 + 64 * j, k0, pt.mat);
+                }
+                if (++stage == kPairStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (aborted) settle_ns(100000);
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool aborted = false;
+        for (int t = cluster; t < P.total_tiles && !aborted; t += nclusters) {
+            const PairTile pt = decode_pair_tile(P, t, 0, sym);
+            const PairClass& C = P.cls[pt.ci];
+            const uint32_t idesc = idesc_bf16_f32(256, pt.ncols, sym ? 0 : 1);
+            if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_flag, P.timeout_ns)) {
+                latch_status(P.status, STATUS_TIMEOUT);
+                abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+            for (int kb = 0; kb < C.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_flag, P.timeout_ns)) {
+                    latch_status(P.status, STATUS_TIMEOUT);
+                    abort_flag = 1;
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = tiles_base + stage * kPairStageBytes;
+                const uint32_t sb = sa + kPairAStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                    const uint64_t bdesc = sym ? smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                               : smem_desc_sw128(sb + kk * 2048, 64 * 128, 1024);
+                    tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+                tc_commit_pair_multicast(&empty_bar[stage], 0x3);
+                if (++stage == kPairStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (aborted) break;
+            tc_commit_pair_multicast(&tfull_bar[acc], 0x3);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        // every MMA issued must finish before TMEM is released
+        tc_commit_pair_multicast(&drain_bar, 0x1);
+        mbar_wait_bounded(&drain_bar, 0, nullptr, P.timeout_ns);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int lg = warp & 3;                       // TMEM lane group of this warp
+        uint8_t* wbase = epi_ptr + lg * kEpiWarpBytes;
+        uint8_t* in_f32[2] = {wbase, wbase + kEpiInSlotBytes};
+        uint8_t* in_b16[2] = {wbase + 4096, wbase + kEpiInSlotBytes + 4096};
+        uint8_t* out_slot = wbase + 2 * kEpiInSlotBytes;   // bf16 direct at +0, bf16 mirror at +2048; or fp32
+        uint64_t* ibar = in_bar[lg];
+        uint32_t in_phase[2] = {0u, 0u};
+        bool in_pending[2] = {false, false};
+        const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
+                                           mapa_shared(smem_u32(&tempty_bar[1]), 0)};
+        const bool has_in = P.mode != MODE_GRAM;
+        const bool final_mode = P.mode == MODE_AXPY_FINAL;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool stores_issued = false;
+        for (int t = cluster; t < P.total_tiles; t += nclusters) {
+            const PairTile pt = decode_pair_tile(P, t, rank, sym);
+            const PairClass& C = P.cls[pt.ci];
+            const int gm = C.mat_base + pt.mat;
+            const int grow0 = pt.rb * 128 + lg * 32;        // first oriented row of this warp
+            const bool warp_rows = pt.rb < C.row_blocks && grow0 < C.m;
+            const int climit = sym ? C.m : C.n;
+            const int nch = pt.ncols / 32;
+            const bool transposed = C.transposed != 0;
+            const CUtensorMap* pmap = final_mode ? &P.p_maps[gm] : nullptr;
+            // a chunk is live when this warp has rows, its columns exist, and (Gram/poly) its
+            // 128-column block is not below the diagonal for this row block
+            auto live = [&](int ch) {
+                const int cc0 = pt.c0 + ch * 32;
+                if (!warp_rows || cc0 >= climit) return false;
+                if (sym && (cc0 >> 7) < pt.rb) return false;
+                return true;
+            };
+            auto issue_in = [&](int ch) {  // lane 0 only
+                const int slot = ch & 1;
+                const int cc0 = pt.c0 + ch * 32;
+                const uint32_t bytes = final_mode ? 4096u + 2048u : 2048u;
+                mbar_arrive_expect_tx(&ibar[slot], bytes);
+                tma_load_3d(in_b16[slot], &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
+                if (final_mode) {
+                    if (transposed) tma_load_2d(in_f32[slot], pmap, &ibar[slot], grow0, cc0);
+                    else tma_load_2d(in_f32[slot], pmap, &ibar[slot], cc0, grow0);
+                }
+                in_pending[slot] = true;
+            };
+            if (has_in && lane == 0) {
+                if (live(0)) issue_in(0);
+                if (nch > 1 && live(1)) issue_in(1);
+            }
+            const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], acc_phase, &abort_flag,
+                                                                         P.timeout_ns));
+            if (!ready) {
+                if (lane == 0) latch_status(P.status, STATUS_TIMEOUT);
+                abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const float s = P.first_iter ? P.inv_norm[gm] : 1.0f;
+            const float sc = final_mode ? P.lr * P.aspect[gm] : 0.f;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + static_cast<uint32_t>(acc * 256);
+            bool failed = false;
+            for (int ch = 0; ch < nch; ++ch) {
+                uint32_t raw_v[32];
+                __syncwarp();
+                tmem_ld_32x32b_x32(t_row + ch * 32, raw_v);
+                tmem_ld_wait();
+                if (ch == nch - 1) {
+                    // the accumulator is no longer read: hand it back to the MMA issuer
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+                }
+                const int slot = ch & 1;
+                const bool lv = live(ch);
+                if (lv) {
+                    const int cc0 = pt.c0 + ch * 32;
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw_v[j]);
+                    if (has_in) {
+                        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ibar[slot], in_phase[slot],
+                                                                                  &abort_flag, P.timeout_ns));
+                        if (!ok) {
+                            if (lane == 0) latch_status(P.status, STATUS_TIMEOUT);
+                            abort_flag = 1;
+                            failed = true;
+                        } else {
+                            in_phase[slot] ^= 1u;
+                            in_pending[slot] = false;
+                        }
+                    }
+                    if (failed) break;
+                    // ---- the epilogue arithmetic, one oriented row (= lane) per thread
+                    if (P.mode == MODE_GRAM) {
+                        const float s2 = s * s;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= s2;
+                    } else {
+                        const uint8_t* xb = in_b16[slot];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(xb + sw64_unit(lane, u));
+                            const float a[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = 8 * u + e;
+                                v[j] = (P.mode == MODE_POLY) ? fmaf(P.cc, v[j], P.cb * a[e]) : s * fmaf(P.ca, a[e], v[j]);
+                            }
+                        }
+                    }
+                    // the previous chunk's stores must have read their shared sources
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+                    if (final_mode) {
+                        // p -= sc O on the fp32 weight subtile, in place
+                        uint8_t* pf = in_f32[slot];
+                        if (!transposed) {
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                float4* q = reinterpret_cast<float4*>(pf + sw128_unit(lane, u));
+                                float4 w = *q;
+                                w.x = fmaf(-sc, v[4 * u + 0], w.x);
+                                w.y = fmaf(-sc, v[4 * u + 1], w.y);
+                                w.z = fmaf(-sc, v[4 * u + 2], w.z);
+                                w.w = fmaf(-sc, v[4 * u + 3], w.w);
+                                *q = w;
+                            }
+                        } else {
+                            // subtile rows are stored rows (= oriented columns j), columns are lanes
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                float* q = reinterpret_cast<float*>(pf + sw128_elem(j, lane));
+                                *q = fmaf(-sc, v[j], *q);
+                            }
+                        }
+                        if (P.dbg_maps) {
+                            if (!transposed) {
+#pragma unroll
+                                for (int u = 0; u < 8; ++u)
+                                    *reinterpret_cast<float4*>(out_slot + sw128_unit(lane, u)) =
+                                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    *reinterpret_cast<float*>(out_slot + sw128_elem(j, lane)) = v[j];
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint4 w;
+                            w.x = pack2(v[8 * u + 0], v[8 * u + 1]);
+                            w.y = pack2(v[8 * u + 2], v[8 * u + 3]);
+                            w.z = pack2(v[8 * u + 4], v[8 * u + 5]);
+                            w.w = pack2(v[8 * u + 6], v[8 * u + 7]);
+                            *reinterpret_cast<uint4*>(out_slot + sw64_unit(lane, u)) = w;
+                        }
+                    }
+                    const bool mirror = sym && (cc0 >> 7) > pt.rb;
+                    if (mirror) {
+                        // transposed subtile: row j (= output row cc0 + j), column lane
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            *reinterpret_cast<__nv_bfloat16*>(out_slot + 2048 + sw64_elem(j, lane)) =
+                                __float2bfloat16_rn(v[j]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (final_mode) {
+                            if (transposed) tma_store_2d(pmap, in_f32[slot], grow0, cc0);
+                            else tma_store_2d(pmap, in_f32[slot], cc0, grow0);
+                            if (P.dbg_maps) {
+                                if (transposed) tma_store_2d(&P.dbg_maps[gm], out_slot, grow0, cc0);
+                                else tma_store_2d(&P.dbg_maps[gm], out_slot, cc0, grow0);
+                            }
+                        } else {
+                            tma_store_3d(&P.tmOut[pt.ci], out_slot, cc0, grow0, pt.mat);
+                            if (mirror) tma_store_3d(&P.tmOut[pt.ci], out_slot + 2048, grow0, cc0, pt.mat);
+                        }
+                        bulk_commit_group();
+                        stores_issued = true;
+                    }
+                }
+                // refill this slot with the chunk two ahead
+                if (has_in && lane == 0 && ch + 2 < nch && live(ch + 2)) {
+                    if (final_mode) bulk_wait_group_read0();  // the p store above reads this slot
+                    issue_in(ch + 2);
+                }
+            }
+            if (failed) break;
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) {
+            // loads still in flight (after an abort) must land before shared memory goes away
+            for (int sl = 0; sl < 2; ++sl)
+                if (in_pending[sl]) mbar_wait_bounded(&ibar[sl], in_phase[sl], nullptr, P.timeout_ns);
+            if (stores_issued) bulk_wait_group0();
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();  // no CTA of the pair touches the other's shared memory or TMEM after this
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+cudaError_t ns_pair_prepare(int* max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(ns_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, ns_pair_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    *max_clusters = n;
+    return cudaSuccess;
+}
+
+cudaError_t launch_ns_pair(const PairParams& p, int clusters, cudaStream_t s) {
+    if (p.total_tiles <= 0 || clusters <= 0) return cudaSuccess;
+    ns_pair_kernel<<<2 * clusters, kGemmThreads, kPairSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace muon

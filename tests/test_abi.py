@@ -64,21 +64,35 @@ def test_init_rejects_bad_configs_before_touching_the_device(L):
 
 
 # ------------------------------------------------------------------ host planner
-def enumerate_tiles(m, n):
-    """Brute-force tile sets of the 128 x 256 tiling: Gram/polynomial tiles cover
-    every 128 x 128 block on or above the diagonal exactly once (tile = row block
-    bi, column blocks cb and cb + 1 for cb = bi, bi + 2, ...); axpy tiles cover X."""
+def enumerate_pair_tiles(m, n):
+    """Brute-force tile sets of the CTA-pair tiling (two 128-row blocks per tile).
+
+    Gram/polynomial: tile (rp, q) = row blocks 2rp, 2rp+1 x column blocks 2q, 2q+1
+    (those that exist), rp <= q.  Every 128 x 128 block on or above the diagonal
+    must be stored by exactly one tile (the lower block of a diagonal tile is not
+    stored).  Axpy: tile (rp, ct) = row blocks 2rp, 2rp+1 x 256 columns from
+    256 ct (128 when fewer than 129 remain).  Returns tile counts and the executed
+    flops per unit K (2 x 256 x N per tile)."""
     rb = math.ceil(m / 128)
-    sym = [(bi, cb) for bi in range(rb) for cb in range(bi, rb, 2)]
-    covered = set()
-    for bi, cb in sym:
-        for c in (cb, cb + 1):
-            if c < rb:
-                assert (bi, c) not in covered
-                covered.add((bi, c))
-    assert covered == {(i, j) for i in range(rb) for j in range(i, rb)}
-    axpy = rb * math.ceil(n / 256)
-    return len(sym), axpy
+    sym, sym_cols = [], 0
+    stored = set()
+    for q in range(math.ceil(rb / 2)):
+        cols = [c for c in (2 * q, 2 * q + 1) if c < rb]
+        for rp in range(q + 1):
+            sym.append((rp, q))
+            sym_cols += 128 * len(cols)
+            for i in (2 * rp, 2 * rp + 1):
+                for c in cols:
+                    if i < rb and i <= c:
+                        assert (i, c) not in stored
+                        stored.add((i, c))
+    assert stored == {(i, j) for i in range(rb) for j in range(i, rb)}
+    axpy, axpy_cols = 0, 0
+    for rp in range(math.ceil(rb / 2)):
+        for c0 in range(0, n, 256):
+            axpy += 1
+            axpy_cols += 256 if n - c0 > 128 else 128
+    return len(sym), axpy, 2 * 256 * sym_cols, 2 * 256 * axpy_cols
 
 
 def expected_plan(shapes, K):
@@ -89,11 +103,11 @@ def expected_plan(shapes, K):
     alg = exe = 0.0
     sym = axpy = 0
     for (m, n, _), G in classes.items():
-        s, a = enumerate_tiles(m, n)
+        s, a, sym_f, axpy_f = enumerate_pair_tiles(m, n)
         sym += G * s
         axpy += G * a
         alg += G * K * (3 * m * m * n + m ** 3)
-        exe += G * K * 2 * 128 * 256 * (s * (n + m) + a * m)
+        exe += G * K * (sym_f * n + sym_f * m + axpy_f * m)   # Gram K = n, polynomial K = m, axpy K = m
     ctas = sum(math.ceil(r / 64) * math.ceil(c / 64) for r, c in shapes)
     elem = sum(22 * r * c for r, c in shapes)
     return len(classes), alg, exe, sym, axpy, ctas, elem
