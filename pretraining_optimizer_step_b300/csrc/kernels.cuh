@@ -123,7 +123,10 @@ cudaError_t ns_gemm_prepare();  // one-time kernel attribute setup
 // last column tile) with tcgen05.mma.cta_group::2: each CTA holds 128 rows of
 // the A operand and N/2 rows of the B operand per pipeline stage, and receives
 // its 128 rows of the accumulator in its own TMEM.
-constexpr int kPairStages = 4;
+#ifndef MUON_PAIR_STAGES
+#define MUON_PAIR_STAGES 4
+#endif
+constexpr int kPairStages = MUON_PAIR_STAGES;
 constexpr int kPairAStageBytes = 128 * 64 * 2;               // 16 KiB: 128 rows x 64 K of bf16
 constexpr int kPairBStageBytes = 128 * 64 * 2;               // 16 KiB: up to 128 B-side rows (N/2)
 constexpr int kPairStageBytes = kPairAStageBytes + kPairBStageBytes;

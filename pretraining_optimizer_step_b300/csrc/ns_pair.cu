@@ -26,11 +26,12 @@
 //   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues the MMAs
 //               (M 256, N 256/128, K 16) and commits to both CTAs' barriers
 //   warps 2..5  epilogue (both CTAs): per warp 32 rows, in chunks of 32 columns.
-//               Inputs (the A or X tile, the fp32 weights) arrive by TMA into two
-//               swizzled shared slots, one chunk ahead; outputs leave by TMA store
-//               from a swizzled shared slot.  Threads touch shared memory only
+//               Inputs (the A or X tile; the fp32 weights in the final launch)
+//               arrive by TMA into a ring of swizzled shared slots, three chunks
+//               ahead (one in the final launch); outputs leave by TMA store from
+//               two alternating swizzled slots.  Threads touch shared memory only
 //               with conflict-free 16-byte vectors (row access) or 4-byte/2-byte
-//               column access of 128-byte rows (transposes).
+//               column access (transposes).
 // Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, raises its
 // abort flag, lets its own copies land, and joins the final cluster barrier.
 #include "kernels.cuh"
@@ -113,7 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     __shared__ __align__(8) uint64_t tfull_bar[2];
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t drain_bar;
-    __shared__ __align__(8) uint64_t in_bar[4][2];
+    __shared__ __align__(8) uint64_t in_bar[4][4];
     __shared__ uint32_t tmem_base_slot;
     __shared__ volatile int abort_flag;
 
@@ -140,10 +141,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty_bar[a], 8);  // one arrive per epilogue warp of both CTAs
         }
         mbar_init(&drain_bar, 1);
-        for (int w = 0; w < 4; ++w) {
-            mbar_init(&in_bar[w][0], 1);
-            mbar_init(&in_bar[w][1], 1);
-        }
+        for (int w = 0; w < 4; ++w)
+            for (int sl = 0; sl < 4; ++sl) mbar_init(&in_bar[w][sl], 1);
         abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
@@ -260,16 +259,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int lg = warp & 3;                       // TMEM lane group of this warp
         uint8_t* wbase = epi_ptr + lg * kEpiWarpBytes;
-        uint8_t* in_f32[2] = {wbase, wbase + kEpiInSlotBytes};
-        uint8_t* in_b16[2] = {wbase + 4096, wbase + kEpiInSlotBytes + 4096};
-        uint8_t* out_slot = wbase + 2 * kEpiInSlotBytes;   // bf16 direct at +0, bf16 mirror at +2048; or fp32
-        uint64_t* ibar = in_bar[lg];
-        uint32_t in_phase[2] = {0u, 0u};
-        bool in_pending[2] = {false, false};
-        const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
-                                           mapa_shared(smem_u32(&tempty_bar[1]), 0)};
         const bool has_in = P.mode != MODE_GRAM;
         const bool final_mode = P.mode == MODE_AXPY_FINAL;
+        // The warp's 16 KiB, by mode:
+        //   final:  2 input slots of {fp32 32x32 weights, bf16 32x32 X} (6 KiB) + 1 output slot (4 KiB)
+        //   others: 4 input slots of bf16 32x32 (2 KiB) + 2 output slots of {bf16 direct, bf16 mirror}
+        // An input slot holds chunk c when c % n_in == slot; loads run n_in - 1 chunks ahead.
+        const int n_in = final_mode ? 2 : 4;
+        const int in_stride = final_mode ? kEpiInSlotBytes : 2048;
+        uint8_t* out_base = wbase + n_in * in_stride;
+        auto in_f32 = [&](int sl) { return wbase + sl * in_stride; };
+        auto in_b16 = [&](int sl) { return wbase + sl * in_stride + (final_mode ? 4096 : 0); };
+        uint64_t* ibar = in_bar[lg];
+        uint32_t in_phase_bits = 0u, in_pending_bits = 0u;
+        uint32_t groups = 0;  // bulk store groups committed by lane 0 (output slot = groups % n_out)
+        const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty_bar[0]), 0);
+        const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty_bar[1]), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
         bool stores_issued = false;
@@ -292,21 +297,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 return true;
             };
             auto issue_in = [&](int ch) {  // lane 0 only
-                const int slot = ch & 1;
+                const int slot = ch % n_in;
                 const int cc0 = pt.c0 + ch * 32;
                 const uint32_t bytes = final_mode ? 4096u + 2048u : 2048u;
                 mbar_arrive_expect_tx(&ibar[slot], bytes);
-                tma_load_3d(in_b16[slot], &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
+                tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 if (final_mode) {
-                    if (transposed) tma_load_2d(in_f32[slot], pmap, &ibar[slot], grow0, cc0);
-                    else tma_load_2d(in_f32[slot], pmap, &ibar[slot], cc0, grow0);
+                    if (transposed) tma_load_2d(in_f32(slot), pmap, &ibar[slot], grow0, cc0);
+                    else tma_load_2d(in_f32(slot), pmap, &ibar[slot], cc0, grow0);
                 }
-                in_pending[slot] = true;
+                in_pending_bits |= 1u << slot;
             };
-            if (has_in && lane == 0) {
-                if (live(0)) issue_in(0);
-                if (nch > 1 && live(1)) issue_in(1);
-            }
+            if (has_in && lane == 0)
+                for (int ch = 0; ch < n_in && ch < nch; ++ch)
+                    if (live(ch)) issue_in(ch);
             const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], acc_phase, &abort_flag,
                                                                          P.timeout_ns));
             if (!ready) {
@@ -328,9 +332,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     // the accumulator is no longer read: hand it back to the MMA issuer
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+                    if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                 }
-                const int slot = ch & 1;
+                const int slot = ch % n_in;
                 const bool lv = live(ch);
                 if (lv) {
                     const int cc0 = pt.c0 + ch * 32;
@@ -338,15 +342,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw_v[j]);
                     if (has_in) {
-                        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ibar[slot], in_phase[slot],
+                        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ibar[slot], (in_phase_bits >> slot) & 1u,
                                                                                   &abort_flag, P.timeout_ns));
                         if (!ok) {
                             if (lane == 0) latch_status(P.status, STATUS_TIMEOUT);
                             abort_flag = 1;
                             failed = true;
                         } else {
-                            in_phase[slot] ^= 1u;
-                            in_pending[slot] = false;
+                            in_phase_bits ^= 1u << slot;
+                            in_pending_bits &= ~(1u << slot);
                         }
                     }
                     if (failed) break;
@@ -356,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] *= s2;
                     } else {
-                        const uint8_t* xb = in_b16[slot];
+                        const uint8_t* xb = in_b16(slot);
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const uint4 w = *reinterpret_cast<const uint4*>(xb + sw64_unit(lane, u));
@@ -369,12 +373,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                             }
                         }
                     }
-                    // the previous chunk's stores must have read their shared sources
-                    if (lane == 0) bulk_wait_group_read0();
+                    // the output slot about to be written must no longer be read by an earlier store
+                    // (final: the single slot; others: the slot of the group before the last)
+                    if (lane == 0) {
+                        if (final_mode) bulk_wait_group_read0();
+                        else bulk_wait_group_read1();
+                    }
                     __syncwarp();
+                    uint8_t* out_slot = out_base + (final_mode ? 0 : (groups & 1u) * 4096);
                     if (final_mode) {
                         // p -= sc O on the fp32 weight subtile, in place
-                        uint8_t* pf = in_f32[slot];
+                        uint8_t* pf = in_f32(slot);
                         if (!transposed) {
 #pragma unroll
                             for (int u = 0; u < 8; ++u) {
@@ -429,8 +438,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         if (final_mode) {
-                            if (transposed) tma_store_2d(pmap, in_f32[slot], grow0, cc0);
-                            else tma_store_2d(pmap, in_f32[slot], cc0, grow0);
+                            if (transposed) tma_store_2d(pmap, in_f32(slot), grow0, cc0);
+                            else tma_store_2d(pmap, in_f32(slot), cc0, grow0);
                             if (P.dbg_maps) {
                                 if (transposed) tma_store_2d(&P.dbg_maps[gm], out_slot, grow0, cc0);
                                 else tma_store_2d(&P.dbg_maps[gm], out_slot, cc0, grow0);
@@ -442,11 +451,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         bulk_commit_group();
                         stores_issued = true;
                     }
+                    ++groups;  // every lane keeps the count (warp-uniform)
                 }
-                // refill this slot with the chunk two ahead
-                if (has_in && lane == 0 && ch + 2 < nch && live(ch + 2)) {
+                // refill this slot with the chunk n_in ahead
+                if (has_in && lane == 0 && ch + n_in < nch && live(ch + n_in)) {
                     if (final_mode) bulk_wait_group_read0();  // the p store above reads this slot
-                    issue_in(ch + 2);
+                    issue_in(ch + n_in);
                 }
             }
             if (failed) break;
@@ -457,8 +467,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         }
         if (lane == 0) {
             // loads still in flight (after an abort) must land before shared memory goes away
-            for (int sl = 0; sl < 2; ++sl)
-                if (in_pending[sl]) mbar_wait_bounded(&ibar[sl], in_phase[sl], nullptr, P.timeout_ns);
+            for (int sl = 0; sl < n_in; ++sl)
+                if ((in_pending_bits >> sl) & 1u) mbar_wait_bounded(&ibar[sl], (in_phase_bits >> sl) & 1u, nullptr, P.timeout_ns);
             if (stores_issued) bulk_wait_group0();
         }
     }

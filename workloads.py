@@ -50,10 +50,16 @@ def layer_shapes(dim: int):
 
 
 def config_shapes(name: str):
-    """Stored (rows, cols) of every matrix of a named workload."""
+    """Stored (rows, cols) of every matrix of a named workload.
+
+    "dNxL" is the first L layers of the dN stack (same shapes, fewer matrices),
+    used to profile a stack's kernels on a small footprint."""
     if name in STACK_DEPTHS:
         depth = STACK_DEPTHS[name]
         return layer_shapes(64 * depth) * depth
+    if name.startswith("d") and "x" in name and name.split("x")[0] in STACK_DEPTHS:
+        base, layers = name.split("x")
+        return layer_shapes(64 * STACK_DEPTHS[base]) * int(layers)
     if name.startswith("sweep_"):
         _, n, kind = name.split("_")
         n = int(n)
