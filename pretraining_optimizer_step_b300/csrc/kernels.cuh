@@ -123,24 +123,26 @@ cudaError_t ns_gemm_prepare();  // one-time kernel attribute setup
 // last column tile) with tcgen05.mma.cta_group::2: each CTA holds 128 rows of
 // the A operand and N/2 rows of the B operand per pipeline stage, and receives
 // its 128 rows of the accumulator in its own TMEM.
-#ifndef MUON_PAIR_STAGES
-#define MUON_PAIR_STAGES 4
-#endif
-constexpr int kPairStages = MUON_PAIR_STAGES;
-constexpr int kPairAStageBytes = 128 * 64 * 2;               // 16 KiB: 128 rows x 64 K of bf16
-constexpr int kPairBStageBytes = 128 * 64 * 2;               // 16 KiB: up to 128 B-side rows (N/2)
-constexpr int kPairStageBytes = kPairAStageBytes + kPairBStageBytes;
+// Each pipeline stage covers 128 of K (8 MMAs of K 16): per CTA two 16 KiB
+// panels of A (128 rows x 64 K, 128B-swizzled) and two of its B half.  Fewer,
+// deeper stages amortise the per-stage barrier round trip of the MMA issuer.
+constexpr int kPairBK = 128;
+constexpr int kPairPanelBytes = 128 * 64 * 2;               // 16 KiB
+constexpr int kPairStageBytes = 4 * kPairPanelBytes;         // 64 KiB
+constexpr int kPairMaxStages = 3;
+// Shared memory by mode: Gram/poly/axpy use 3 stages + 8 KiB of epilogue slots per
+// warp; the final launch 2 stages + 24 KiB per warp (fp32 weight subtiles).
 constexpr int kEpiInSlotBytes = 6144;                        // fp32 32x32 (4 KiB) + bf16 32x32 (2 KiB)
-constexpr int kEpiOutSlotBytes = 4096;                       // bf16 32x32 direct + mirror, or fp32 32x32
-constexpr int kEpiWarpBytes = 2 * kEpiInSlotBytes + kEpiOutSlotBytes;
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 4 * kEpiWarpBytes + 1024;
+constexpr int kPairSmemBytes = 224 * 1024 + 1024;
+static_assert(3 * kPairStageBytes + 4 * 8192 <= 224 * 1024, "stage + epilogue layout");
+static_assert(2 * kPairStageBytes + 4 * 24576 <= 224 * 1024, "stage + epilogue layout (final)");
 
 struct PairClass {
     int m, n;             // oriented X is m x n (m <= n)
     int nmats;
     int tile_begin;       // first pair tile of this class in the launch
     int tiles_per_mat;    // pair tiles per matrix
-    int k_blocks;         // ceil(K / 64)
+    int k_blocks;         // ceil(K / 128)
     int row_blocks;       // ceil(m / 128)
     int col_groups;       // Gram/poly: ceil(row_blocks / 2) column pairs; axpy: ceil(n / 256) column tiles
     int transposed;       // stored matrix is n x m
@@ -149,7 +151,8 @@ struct PairClass {
 
 struct PairParams {
     CUtensorMap tmA[kMaxClasses];    // A side, K-major, box 64 (K) x 128 rows, 128B swizzle
-    CUtensorMap tmB[kMaxClasses];    // B side: Gram/poly K-major box 64 x 64; axpy MN-major box 64 cols x 64 K
+    CUtensorMap tmB[kMaxClasses];    // B side: Gram/poly K-major box 64 x 64 (N = 128 tiles; N = 256 tiles
+                                     // use tmA); axpy MN-major box 64 cols x 128 K
     CUtensorMap tmIn[kMaxClasses];   // epilogue input (poly: A, axpy: X), bf16 box 32 x 32, 64B swizzle
     CUtensorMap tmOut[kMaxClasses];  // epilogue output (gram: A, poly: B, axpy: X'), bf16 box 32 x 32, 64B swizzle
     PairClass cls[kMaxClasses];

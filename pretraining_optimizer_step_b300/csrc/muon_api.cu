@@ -33,7 +33,7 @@ struct ClassPlan {
     __nv_bfloat16* B = nullptr;
     CUtensorMap tmXk[2], tmXmn[2], tmAk, tmBk;
     // CTA-pair kernel: B-side K-major maps (box 64 x 64) and epilogue subtile maps (bf16 32 x 32)
-    CUtensorMap tmXk64[2], tmAk64, epiX[2], epiA, epiB;
+    CUtensorMap tmXk64[2], tmAk64, tmXmn128[2], epiX[2], epiA, epiB;
     int row_blocks = 0, col_tiles = 0, sym_tiles = 0, axpy_tiles = 0;
     int col_pairs = 0, sym_pair_tiles = 0, axpy_pair_tiles = 0;
 };
@@ -300,6 +300,9 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
         for (int pp = 0; pp < 2 && st == MUON_OK; ++pp) {
             st = encode_map_ex(ctx->encode, &cp.tmXk64[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, kBK, 64,
                                CU_TENSOR_MAP_SWIZZLE_128B);
+            if (st == MUON_OK)
+                st = encode_map_ex(ctx->encode, &cp.tmXmn128[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 64, kPairBK,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
             if (st == MUON_OK)
                 st = encode_map_ex(ctx->encode, &cp.epiX[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 32, 32,
                                    CU_TENSOR_MAP_SWIZZLE_64B);
@@ -687,7 +690,7 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
                         if (mode == MODE_GRAM) {
                             C.tiles_per_mat = cp.sym_pair_tiles;
                             C.col_groups = cp.col_pairs;
-                            C.k_blocks = (cp.n + kBK - 1) / kBK;
+                            C.k_blocks = (cp.n + kPairBK - 1) / kPairBK;
                             pp.tmA[k] = cp.tmXk[pin];
                             pp.tmB[k] = cp.tmXk64[pin];
                             pp.tmIn[k] = cp.epiX[pin];
@@ -695,7 +698,7 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
                         } else if (mode == MODE_POLY) {
                             C.tiles_per_mat = cp.sym_pair_tiles;
                             C.col_groups = cp.col_pairs;
-                            C.k_blocks = (cp.m + kBK - 1) / kBK;
+                            C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
                             pp.tmA[k] = cp.tmAk;
                             pp.tmB[k] = cp.tmAk64;
                             pp.tmIn[k] = cp.epiA;
@@ -703,9 +706,9 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
                         } else {
                             C.tiles_per_mat = cp.axpy_pair_tiles;
                             C.col_groups = cp.col_tiles;
-                            C.k_blocks = (cp.m + kBK - 1) / kBK;
+                            C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
                             pp.tmA[k] = cp.tmBk;
-                            pp.tmB[k] = cp.tmXmn[pin];
+                            pp.tmB[k] = cp.tmXmn128[pin];
                             pp.tmIn[k] = cp.epiX[pin];
                             pp.tmOut[k] = cp.epiX[pout];
                         }

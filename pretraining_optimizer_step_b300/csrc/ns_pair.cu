@@ -21,15 +21,16 @@
 //   axpy:      tile = row blocks (2 rp, 2 rp + 1) x columns [256 ct, 256 ct + N).
 //
 // CTA layout (192 threads, persistent over the pair tiles):
-//   warp 0      TMA producer (both CTAs): 4-stage ring of {A 128 x 64, B-half <= 128 x 64};
-//               the loads of both CTAs complete on the even CTA's mbarrier
-//   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues the MMAs
-//               (M 256, N 256/128, K 16) and commits to both CTAs' barriers
+//   warp 0      TMA producer (both CTAs): ring of 3 stages (2 in the final launch) of
+//               {A 128 x 128, B-half <= 128 x 128} bf16 as 64-wide K panels; the loads
+//               of both CTAs complete on the even CTA's mbarrier
+//   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues 8 MMAs
+//               (M 256, N 256/128, K 16) per stage and commits to both CTAs' barriers
 //   warps 2..5  epilogue (both CTAs): per warp 32 rows, in chunks of 32 columns.
 //               Inputs (the A or X tile; the fp32 weights in the final launch)
-//               arrive by TMA into a ring of swizzled shared slots, three chunks
-//               ahead (one in the final launch); outputs leave by TMA store from
-//               two alternating swizzled slots.  Threads touch shared memory only
+//               arrive by TMA into a ring of swizzled shared slots, one chunk
+//               ahead (two in the final launch); outputs leave by TMA store from
+//               swizzled slots.  Threads touch shared memory only
 //               with conflict-free 16-byte vectors (row access) or 4-byte/2-byte
 //               column access (transposes).
 // Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, raises its
@@ -109,8 +110,8 @@ __device__ __forceinline__ void settle_ns(uint64_t ns) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     ns_pair_kernel(const __grid_constant__ PairParams P) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kPairStages];
-    __shared__ __align__(8) uint64_t empty_bar[kPairStages];
+    __shared__ __align__(8) uint64_t full_bar[kPairMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kPairMaxStages];
     __shared__ __align__(8) uint64_t tfull_bar[2];
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t drain_bar;
@@ -121,7 +122,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t tiles_base = (raw + 1023u) & ~1023u;
     uint8_t* tiles_ptr = smem_raw + (tiles_base - raw);
-    uint8_t* epi_ptr = tiles_ptr + kPairStages * kPairStageBytes;
+    const bool final_mode = P.mode == MODE_AXPY_FINAL;
+    const int nstages = final_mode ? 2 : 3;
+    const int epi_warp_bytes = final_mode ? 24576 : 8192;
+    uint8_t* epi_ptr = tiles_ptr + nstages * kPairStageBytes;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -132,7 +136,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const bool sym = (P.mode == MODE_GRAM || P.mode == MODE_POLY);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPairStages; ++s) {
+        for (int s = 0; s < kPairMaxStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
@@ -173,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const CUtensorMap* mB = &P.tmB[pt.ci];
             const int half = pt.ncols >> 1;             // this CTA's B-side rows/columns: 64 or 128
             const int b0 = pt.c0 + rank * half;         // first of them
-            const uint32_t total_bytes = 2u * (kPairAStageBytes + static_cast<uint32_t>(half) * kBK * 2u);
+            const uint32_t total_bytes = 2u * (2u * kPairPanelBytes + static_cast<uint32_t>(half) * kPairBK * 2u);
             for (int kb = 0; kb < C.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, P.timeout_ns)) {
                     latch_status(P.status, STATUS_TIMEOUT);
@@ -181,23 +185,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     aborted = true;
                     break;
                 }
-                uint8_t* sa = tiles_ptr + stage * kPairStageBytes;
-                uint8_t* sb = sa + kPairAStageBytes;
-                const int k0 = kb * kBK;
+                uint8_t* sa = tiles_ptr + stage * kPairStageBytes;  // A: K panels at +0, +16 KiB
+                uint8_t* sb = sa + 2 * kPairPanelBytes;               // B half: panels at +32, +48 KiB
+                const int k0 = kb * kPairBK;
                 const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
                 if (leader) mbar_arrive_expect_tx(&full_bar[stage], total_bytes);
-                if (P.inject_lost_load && leader && !injected && cluster == 0) {
-                    injected = true;  // test hook: this A slice never arrives
+                for (int h = 0; h < 2; ++h) {
+                    if (P.inject_lost_load && leader && !injected && cluster == 0) {
+                        injected = true;  // test hook: this A panel never arrives
+                    } else {
+                        tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, k0 + 64 * h, pt.rb * 128, pt.mat);
+                    }
+                }
+                if (sym) {
+                    // K-major B half: 128 rows (box of tmA) or 64 rows (box of tmB) per K panel
+                    const CUtensorMap* mBs = half == 128 ? mA : mB;
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d_pair(sb + h * kPairPanelBytes, mBs, bar, k0 + 64 * h, b0, pt.mat);
                 } else {
-                    tma_load_3d_pair(sa, mA, bar, k0, pt.rb * 128, pt.mat);
+                    // MN-major X: one 64-column x 128-K panel per 64 columns of the B half
+                    for (int j = 0; j < half / 64; ++j)
+                        tma_load_3d_pair(sb + j * kPairPanelBytes, mB, bar, b0 + 64 * j, k0, pt.mat);
                 }
-                for (int j = 0; j < half / 64; ++j) {
-                    if (sym)
-                        tma_load_3d_pair(sb + j * (64 * 128), mB, bar, k0, b0 + 64 * j, pt.mat);
-                    else
-                        tma_load_3d_pair(sb + j * (64 * 128), mB, bar, b0 + 64 * j, k0, pt.mat);
-                }
-                if (++stage == kPairStages) {
+                if (++stage == nstages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -231,16 +241,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t sa = tiles_base + stage * kPairStageBytes;
-                const uint32_t sb = sa + kPairAStageBytes;
+                const uint32_t sb = sa + 2 * kPairPanelBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                    const uint64_t bdesc = sym ? smem_desc_sw128(sb + kk * 32, 16, 1024)
-                                               : smem_desc_sw128(sb + kk * 2048, 64 * 128, 1024);
+                for (int kk = 0; kk < kPairBK / 16; ++kk) {
+                    const uint32_t kpan = (kk >> 2) * kPairPanelBytes + (kk & 3) * 32;  // K-major: panel, 32 B per K 16
+                    const uint64_t adesc = smem_desc_sw128(sa + kpan, 16, 1024);
+                    const uint64_t bdesc = sym ? smem_desc_sw128(sb + kpan, 16, 1024)
+                                               : smem_desc_sw128(sb + kk * 2048, kPairPanelBytes, 1024);
                     tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
                 tc_commit_pair_multicast(&empty_bar[stage], 0x3);
-                if (++stage == kPairStages) {
+                if (++stage == nstages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -258,15 +269,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int lg = warp & 3;                       // TMEM lane group of this warp
-        uint8_t* wbase = epi_ptr + lg * kEpiWarpBytes;
+        uint8_t* wbase = epi_ptr + lg * epi_warp_bytes;
         const bool has_in = P.mode != MODE_GRAM;
-        const bool final_mode = P.mode == MODE_AXPY_FINAL;
-        // The warp's 16 KiB, by mode:
-        //   final:  2 input slots of {fp32 32x32 weights, bf16 32x32 X} (6 KiB) + 1 output slot (4 KiB)
-        //   others: 4 input slots of bf16 32x32 (2 KiB) + 2 output slots of {bf16 direct, bf16 mirror}
-        // An input slot holds chunk c when c % n_in == slot; loads run n_in - 1 chunks ahead.
-        const int n_in = final_mode ? 2 : 4;
+        // The warp's epilogue slots, by mode (an input slot holds chunk c when c % n_in == slot;
+        // loads run n_in - 1 chunks ahead; output slots alternate per committed store group):
+        //   final (24 KiB): 3 input slots of {fp32 32x32 weights, bf16 32x32 X} (6 KiB) + 1 output
+        //                   slot (fp32 O for the debug copy)
+        //   gram  (8 KiB):  2 output slots of {bf16 direct, bf16 mirror}
+        //   poly  (8 KiB):  2 bf16 input slots + 1 output slot of {direct, mirror}
+        //   axpy  (8 KiB):  2 bf16 input slots + 2 output slots of bf16 direct
+        const int n_in = final_mode ? 3 : (has_in ? 2 : 0);
         const int in_stride = final_mode ? kEpiInSlotBytes : 2048;
+        const int n_out = (P.mode == MODE_GRAM || P.mode == MODE_AXPY) ? 2 : 1;
+        const int out_stride = (P.mode == MODE_AXPY) ? 2048 : 4096;
         uint8_t* out_base = wbase + n_in * in_stride;
         auto in_f32 = [&](int sl) { return wbase + sl * in_stride; };
         auto in_b16 = [&](int sl) { return wbase + sl * in_stride + (final_mode ? 4096 : 0); };
@@ -296,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 if (sym && (cc0 >> 7) < pt.rb) return false;
                 return true;
             };
-            auto issue_in = [&](int ch) {  // lane 0 only
+            auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0
                 const int slot = ch % n_in;
                 const int cc0 = pt.c0 + ch * 32;
                 const uint32_t bytes = final_mode ? 4096u + 2048u : 2048u;
@@ -334,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                 }
-                const int slot = ch % n_in;
+                const int slot = n_in > 0 ? ch % n_in : 0;
                 const bool lv = live(ch);
                 if (lv) {
                     const int cc0 = pt.c0 + ch * 32;
@@ -376,11 +391,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     // the output slot about to be written must no longer be read by an earlier store
                     // (final: the single slot; others: the slot of the group before the last)
                     if (lane == 0) {
-                        if (final_mode) bulk_wait_group_read0();
+                        if (n_out == 1) bulk_wait_group_read0();
                         else bulk_wait_group_read1();
                     }
                     __syncwarp();
-                    uint8_t* out_slot = out_base + (final_mode ? 0 : (groups & 1u) * 4096);
+                    uint8_t* out_slot = out_base + (n_out == 1 ? 0u : (groups & 1u) * out_stride);
                     if (final_mode) {
                         // p -= sc O on the fp32 weight subtile, in place
                         uint8_t* pf = in_f32(slot);
