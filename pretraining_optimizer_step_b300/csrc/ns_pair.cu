@@ -5,10 +5,13 @@
 // three launches of this kernel over every matrix of the step (grouped by
 // oriented shape class); the modes and their epilogues are those of
 // ns_gemm.cu:
-//   MODE_GRAM        A = s^2 X X^T          tiles on/above the diagonal, mirrored on store
-//   MODE_POLY        B = b A + c A A        A symmetric: A A = A A^T, same operand both sides
-//   MODE_AXPY        X' = s (a X + B X)     X read MN-major as the B operand
-//   MODE_AXPY_FINAL  O = s (a X + B X) in fp32, p -= lr sqrt(max(1, r/c)) O
+//   MODE_GRAM        A = s^2 X X^T               tiles on/above the diagonal, mirrored on store
+//   MODE_POLY        B' = b A + c A A + a I      A symmetric: A A = A A^T, same operand both sides
+//   MODE_AXPY        X' = s B' X                 X read MN-major as the B operand
+//   MODE_AXPY_FINAL  O = s B' X in fp32, p -= lr sqrt(max(1, r/c)) O
+// Folding a I into the polynomial makes a X + B X = (B + a I) X a plain product, so the
+// axpy epilogues read nothing but the accumulator (and the weights in the final launch);
+// the only numerical change is one bf16 rounding of B's diagonal entries plus a.
 //
 // A cluster of two CTAs (one per SM) computes a 256 x N tile with
 // tcgen05.mma.cta_group::2: CTA rank r holds rows [128 r, 128 r + 128) of the A
@@ -270,21 +273,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int lg = warp & 3;                       // TMEM lane group of this warp
         uint8_t* wbase = epi_ptr + lg * epi_warp_bytes;
-        const bool has_in = P.mode != MODE_GRAM;
+        const bool has_in = P.mode == MODE_POLY || final_mode;
         // The warp's epilogue slots, by mode (an input slot holds chunk c when c % n_in == slot;
         // loads run n_in - 1 chunks ahead; output slots alternate per committed store group):
-        //   final (24 KiB): 3 input slots of {fp32 32x32 weights, bf16 32x32 X} (6 KiB) + 1 output
-        //                   slot (fp32 O for the debug copy)
+        //   final (24 KiB): 4 input slots of fp32 32x32 weights (4 KiB) + 1 output slot (fp32 O,
+        //                   for the debug copy)
         //   gram  (8 KiB):  2 output slots of {bf16 direct, bf16 mirror}
-        //   poly  (8 KiB):  2 bf16 input slots + 1 output slot of {direct, mirror}
-        //   axpy  (8 KiB):  2 bf16 input slots + 2 output slots of bf16 direct
-        const int n_in = final_mode ? 3 : (has_in ? 2 : 0);
-        const int in_stride = final_mode ? kEpiInSlotBytes : 2048;
-        const int n_out = (P.mode == MODE_GRAM || P.mode == MODE_AXPY) ? 2 : 1;
+        //   poly  (8 KiB):  2 bf16 input slots (A) + 1 output slot of {direct, mirror}
+        //   axpy  (8 KiB):  4 output slots of bf16 direct
+        const int n_in = final_mode ? 4 : (has_in ? 2 : 0);
+        const int in_stride = final_mode ? 4096 : 2048;
+        const int n_out = P.mode == MODE_GRAM ? 2 : (P.mode == MODE_AXPY ? 4 : 1);
         const int out_stride = (P.mode == MODE_AXPY) ? 2048 : 4096;
         uint8_t* out_base = wbase + n_in * in_stride;
         auto in_f32 = [&](int sl) { return wbase + sl * in_stride; };
-        auto in_b16 = [&](int sl) { return wbase + sl * in_stride + (final_mode ? 4096 : 0); };
+        auto in_b16 = [&](int sl) { return wbase + sl * in_stride; };
         uint64_t* ibar = in_bar[lg];
         uint32_t in_phase_bits = 0u, in_pending_bits = 0u;
         uint32_t groups = 0;  // bulk store groups committed by lane 0 (output slot = groups % n_out)
@@ -314,12 +317,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0
                 const int slot = ch % n_in;
                 const int cc0 = pt.c0 + ch * 32;
-                const uint32_t bytes = final_mode ? 4096u + 2048u : 2048u;
-                mbar_arrive_expect_tx(&ibar[slot], bytes);
-                tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 if (final_mode) {
+                    mbar_arrive_expect_tx(&ibar[slot], 4096u);
                     if (transposed) tma_load_2d(in_f32(slot), pmap, &ibar[slot], grow0, cc0);
                     else tma_load_2d(in_f32(slot), pmap, &ibar[slot], cc0, grow0);
+                } else {
+                    mbar_arrive_expect_tx(&ibar[slot], 2048u);
+                    tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 }
                 in_pending_bits |= 1u << slot;
             };
@@ -374,8 +378,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         const float s2 = s * s;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] *= s2;
-                    } else {
+                    } else if (P.mode == MODE_POLY) {
                         const uint8_t* xb = in_b16(slot);
+                        const bool diag = cc0 == grow0;  // this 32 x 32 block holds diagonal entries
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const uint4 w = *reinterpret_cast<const uint4*>(xb + sw64_unit(lane, u));
@@ -384,18 +389,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int j = 8 * u + e;
-                                v[j] = (P.mode == MODE_POLY) ? fmaf(P.cc, v[j], P.cb * a[e]) : s * fmaf(P.ca, a[e], v[j]);
+                                v[j] = fmaf(P.cc, v[j], P.cb * a[e]) + ((diag && j == lane) ? P.ca : 0.0f);
                             }
                         }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= s;
                     }
                     // the output slot about to be written must no longer be read by an earlier store
                     // (final: the single slot; others: the slot of the group before the last)
                     if (lane == 0) {
                         if (n_out == 1) bulk_wait_group_read0();
-                        else bulk_wait_group_read1();
+                        else if (n_out == 2) bulk_wait_group_read1();
+                        else bulk_wait_group_read3();
                     }
                     __syncwarp();
-                    uint8_t* out_slot = out_base + (n_out == 1 ? 0u : (groups & 1u) * out_stride);
+                    uint8_t* out_slot = out_base + (groups % static_cast<uint32_t>(n_out)) * out_stride;
                     if (final_mode) {
                         // p -= sc O on the fp32 weight subtile, in place
                         uint8_t* pf = in_f32(slot);

@@ -246,6 +246,9 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 __device__ __forceinline__ void bulk_wait_group_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_group_read3() {
+    asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+}
 // Wait until every committed bulk group has completed (its global writes are done).
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
