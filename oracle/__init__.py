@@ -1,4 +1,5 @@
-"""fp64 CPU oracle of the Muon optimizer step (ctypes wrapper around muon_oracle.c).
+"""fp64 CPU oracle of the Muon optimizer step and of the AdamW step for the
+parameters Muon does not take (ctypes wrapper around muon_oracle.c).
 
 TEST INFRASTRUCTURE ONLY: tests/, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` may import this package; the product library never
@@ -64,6 +65,9 @@ def bind(lib):
     lib.oracle_muon_matrix.restype = ctypes.c_int
     lib.oracle_frobenius.argtypes = [ctypes.c_long, f64p]
     lib.oracle_frobenius.restype = ctypes.c_double
+    lib.oracle_adamw.argtypes = [ctypes.c_long, f32p, f32p, f32p, f32p, ctypes.c_double, ctypes.c_double,
+                                 ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int]
+    lib.oracle_adamw.restype = None
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
     return lib
@@ -156,3 +160,16 @@ def muon_matrix(p, g, m, lr, beta, nesterov=True, ns_steps=None, coeffs=DEFAULT_
     if rc != 0:
         raise MemoryError("oracle allocation failed")
     return p_out, m_out, O
+
+
+def adamw(p, g, m, v, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=1):
+    """One AdamW step on one tensor (copies in, returns (p', m', v') as float32 arrays)."""
+    p = np.array(p, dtype=np.float32, order="C", copy=True)
+    m = np.array(m, dtype=np.float32, order="C", copy=True)
+    v = np.array(v, dtype=np.float32, order="C", copy=True)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    if int(step) < 1:
+        raise ValueError("step counts from 1")
+    _load().oracle_adamw(p.size, p.reshape(-1), g.reshape(-1), m.reshape(-1), v.reshape(-1), float(lr),
+                         float(beta1), float(beta2), float(eps), float(weight_decay), int(step))
+    return p, m, v

@@ -200,3 +200,31 @@ int oracle_muon_matrix(int r, int c, const float* p, const float* g, const float
     if (!O_out) free(O);
     return rcode;
 }
+
+/*
+ * AdamW for the parameters the optimizer split sends away from Muon (the
+ * dev.to page's table in section "2. ตัวปรับปรุง Muon": embeddings, lm_head
+ * and scalar parameters go to AdamW).  The pages give no formula; the reading
+ * is decoupled weight decay with bias-corrected moments, step t >= 1:
+ *   p  <- p (1 - lr wd)
+ *   m  <- beta1 m + (1 - beta1) g
+ *   v  <- beta2 v + (1 - beta2) g^2
+ *   p  <- p - (lr / (1 - beta1^t)) m / (sqrt(v / (1 - beta2^t)) + eps)
+ * Everything in double; p, m, v are rounded to float where they are stored.
+ */
+void oracle_adamw(long n_elem, float* p, const float* g, float* m, float* v, double lr, double beta1,
+                  double beta2, double eps, double weight_decay, int step) {
+    const double bc1 = 1.0 - pow(beta1, (double)step);
+    const double bc2 = 1.0 - pow(beta2, (double)step);
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < n_elem; ++e) {
+        double pd = (double)p[e] * (1.0 - lr * weight_decay);
+        const double gd = (double)g[e];
+        const double md = beta1 * (double)m[e] + (1.0 - beta1) * gd;
+        const double vd = beta2 * (double)v[e] + (1.0 - beta2) * gd * gd;
+        pd -= (lr / bc1) * md / (sqrt(vd / bc2) + eps);
+        p[e] = (float)pd;
+        m[e] = (float)md;
+        v[e] = (float)vd;
+    }
+}
