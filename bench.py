@@ -356,6 +356,26 @@ def run_ours(args, rank, world, local_rank):
                     "avg_launch_ms": mom_ms / max(mom_launches, 1)}
     phase_ms = {k: v[0] / args.steps for k, v in kt.items()}
 
+    # ---- AdamW over the same model's non-matrix parameters (embedding, lm_head,
+    # scalars): one multi-tensor launch per step, HBM-bound at 28 bytes per element
+    adamw = None
+    if wl in workloads.STACK_DEPTHS:
+        ap, ag, am, av, ashapes = workloads.make_adamw_set(wl, dev, seed=seed)
+        a_args = mu.AdamWArgs(ap, ag, am, av)
+        a_elems = sum(int(t.numel()) for t in ap)
+        a_hp = dict(lr=3e-3, beta1=0.8, beta2=0.95, eps=1e-8, weight_decay=0.01)
+        for k in range(args.warmup):
+            mu.muon_adamw_step(a_args, step=k + 1, stream=stream, **a_hp)
+        a_ms = timed(args.steps, lambda k: mu.muon_adamw_step(a_args, step=args.warmup + k + 1, stream=stream,
+                                                              **a_hp)) / args.steps
+        a_gbs = 28.0 * a_elems / (a_ms * 1e-3) / 1e9
+        adamw = {"kernel": "adamw_kernel", "tensors": len(ap), "elements": a_elems, "ms_per_step": a_ms,
+                 "bound": "hbm", "achieved": a_gbs, "peak": peak_bw, "unit": "GB/s", "frac": a_gbs / peak_bw,
+                 "alg_bytes_per_element": 28,
+                 "set": "token embedding and untied lm_head (32768 x d each), 2 scalars per layer, smear gate, "
+                        "backout lambda; lr 3e-3, betas (0.8, 0.95), eps 1e-8, wd 0.01"}
+        del ap, ag, am, av
+
     # ---- end to end through the C ABI with host buffers.  Every step uploads its
     # gradients from pinned host memory and downloads the updated weights to pinned
     # host memory, all inside the timed region.  The copies are pipelined across
@@ -447,7 +467,7 @@ def run_ours(args, rank, world, local_rank):
                            "state_dtype": "fp32 p/g/m; bf16 Newton-Schulz operands, fp32 accumulation"},
                 "ns_tflops": ns_tflops, "frac_of_bf16_peak": ns_tflops / peak_tf_sus, "frac_of_bf16_burst_peak": ns_tflops / peak_tf,
                 "phase_ms_per_step": phase_ms, "timed_ms_with_kernel_events": timed_ms2 / args.steps,
-                "roofline": roofline, "roofline_elementwise": roofline_hbm, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "roofline_elementwise": roofline_hbm, "adamw": adamw, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clocks.summary(), "gpu_launches": info["launches"] * args.steps,
                 "workspace_bytes": info["workspace_bytes"]}
         print(json.dumps(line), flush=True)

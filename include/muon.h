@@ -200,6 +200,36 @@ MUON_API muon_status muon_debug_copy_ns_output(int mat, float* dst_device, muon_
 MUON_API muon_status muon_debug_copy_norms(float* dst_host, int n);
 
 /*
+ * AdamW step for the parameters Muon does not take.  The optimizer split of
+ * the method ("Train your own ChatGPT" on dev.to, section "2. ตัวปรับปรุง Muon",
+ * optimizer table; the apidog.com page, same section) sends 2-D matrices to
+ * Muon and embeddings, lm_head and scalar parameters to AdamW.  The pages name
+ * AdamW without a formula; this library takes decoupled weight decay with
+ * bias-corrected moments, step t >= 1:
+ *
+ *   p <- p (1 - lr weight_decay)
+ *   m <- beta1 m + (1 - beta1) g            (exp_avg)
+ *   v <- beta2 v + (1 - beta2) g^2          (exp_avg_sq)
+ *   p <- p - (lr / (1 - beta1^t)) m / (sqrt(v / (1 - beta2^t)) + eps)
+ *
+ * in fp32 (the bias corrections in fp64 on the host).
+ *   params[i], grads[i], exp_avg[i], exp_avg_sq[i]: device float32 arrays of
+ *     numels[i] elements (any shape, contiguous), 16-byte aligned
+ *     (MUON_ERR_MISALIGNED); params, exp_avg, exp_avg_sq are updated in place,
+ *     grads are read only; all caller-owned.  numels[i] >= 0 (0 is skipped).
+ *   beta1, beta2 in [0, 1); eps >= 0; lr, weight_decay finite; step >= 1.
+ * All tensors of a call go into one launch (128 tensors per launch), enqueued
+ * on `stream`.  Needs no muon_init; the current device must be sm_103
+ * (MUON_ERR_UNSUPPORTED_DEVICE).  Errors: MUON_ERR_INVALID_ARG,
+ * MUON_ERR_MISALIGNED, MUON_ERR_UNSUPPORTED_DEVICE, MUON_ERR_CUDA; on an
+ * argument error nothing is enqueued.
+ */
+MUON_API muon_status muon_adamw_step(float* const params[], const float* const grads[], float* const exp_avg[],
+                                     float* const exp_avg_sq[], const long long numels[], int n_tensors,
+                                     float lr, float beta1, float beta2, float eps, float weight_decay, int step,
+                                     muon_stream_t stream);
+
+/*
  * Momentum + norm pass without any allocation.  (The pages have no counterpart:
  * this entry point exists for callers, not for the method.)
  *

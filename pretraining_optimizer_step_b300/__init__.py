@@ -107,9 +107,13 @@ def lib():
         L.muon_momentum_norm_noalloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                                  vp, ctypes.POINTER(muon_shape), ctypes.c_int, ctypes.c_float,
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_double, vp]
+        L.muon_adamw_step.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                      ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_longlong), ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_float, ctypes.c_int, vp]
         for name in ("muon_init", "muon_step", "muon_destroy", "muon_get_status", "muon_get_step_info",
                      "muon_kernel_times", "muon_debug_copy_ns_output", "muon_debug_copy_norms",
-                     "muon_plan_query", "muon_momentum_norm_noalloc"):
+                     "muon_plan_query", "muon_momentum_norm_noalloc", "muon_adamw_step"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -228,6 +232,37 @@ def muon_debug_copy_norms(n: int):
     buf = (ctypes.c_float * max(n, 1))()
     _check(lib().muon_debug_copy_norms(buf, int(n)), "muon_debug_copy_norms")
     return [buf[i] for i in range(n)]
+
+
+class AdamWArgs:
+    """Pre-marshalled pointer and size arrays for repeated muon_adamw_step calls."""
+
+    def __init__(self, params: Sequence, grads: Sequence, exp_avg: Sequence, exp_avg_sq: Sequence,
+                 numels: Optional[Sequence[int]] = None):
+        n = len(params)
+        if not (len(grads) == len(exp_avg) == len(exp_avg_sq) == n):
+            raise ValueError("params, grads, exp_avg and exp_avg_sq must have the same length")
+        if numels is None:
+            numels = [int(x.numel()) for x in params]
+        vp = ctypes.c_void_p
+        self.n = n
+        self.params = (vp * max(n, 1))(*[_ptr(x) for x in params])
+        self.grads = (vp * max(n, 1))(*[_ptr(x) for x in grads])
+        self.exp_avg = (vp * max(n, 1))(*[_ptr(x) for x in exp_avg])
+        self.exp_avg_sq = (vp * max(n, 1))(*[_ptr(x) for x in exp_avg_sq])
+        self.numels = (ctypes.c_longlong * max(n, 1))(*[int(k) for k in numels])
+
+
+def muon_adamw_step(params, grads=None, exp_avg=None, exp_avg_sq=None, lr: float = 1e-3,
+                    beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.01,
+                    step: int = 1, stream=None, numels=None, check: bool = True) -> int:
+    """Enqueue one AdamW step over a list of fp32 tensors (see include/muon.h).
+    ``params`` may be a prepared AdamWArgs."""
+    a = params if isinstance(params, AdamWArgs) else AdamWArgs(params, grads, exp_avg, exp_avg_sq, numels)
+    st = lib().muon_adamw_step(a.params, a.grads, a.exp_avg, a.exp_avg_sq, a.numels, a.n, float(lr),
+                               float(beta1), float(beta2), float(eps), float(weight_decay), int(step),
+                               _stream(stream))
+    return _check(st, "muon_adamw_step") if check else st
 
 
 def muon_momentum_norm_noalloc(grads, momentum_bufs, x0_out, norms_out, beta: float = 0.95,

@@ -188,3 +188,24 @@ def test_noalloc_limits_are_checked_before_the_device(L):
     # within the limits the call reaches the device check (none here)
     assert mu.muon_momentum_norm_noalloc([fake], [fake], [fake], norms, shapes=[(64, 64)],
                                          check=False) == mu.MUON_ERR_UNSUPPORTED_DEVICE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="passes fake pointers; host-side checks only")
+def test_adamw_arguments_are_checked_before_the_device(L):
+    fake = 1 << 20
+    args = mu.AdamWArgs([fake], [fake], [fake], [fake], numels=[64])
+    assert mu.muon_adamw_step(args, step=0, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_adamw_step(args, beta1=1.5, check=False) == mu.MUON_ERR_INVALID_ARG
+    bad = mu.AdamWArgs([fake + 8], [fake], [fake], [fake], numels=[64])
+    assert mu.muon_adamw_step(bad, check=False) == mu.MUON_ERR_MISALIGNED
+    neg = mu.AdamWArgs([fake], [fake], [fake], [fake], numels=[-1])
+    assert mu.muon_adamw_step(neg, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_adamw_step([], [], [], [], check=False) == mu.MUON_OK
+    # valid arguments reach the device check (no device here)
+    assert mu.muon_adamw_step(args, check=False) == mu.MUON_ERR_UNSUPPORTED_DEVICE
+
+
+def test_adamw_set_shapes():
+    shapes = workloads.adamw_shapes("d26")
+    assert shapes[0] == (32768, 1664) and shapes[1] == (32768, 1664)
+    assert sum(math.prod(s) for s in shapes) == 2 * 32768 * 1664 + 52 + 24 + 1

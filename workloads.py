@@ -116,6 +116,30 @@ def make_stack(name: str, device="cpu", seed: int = 0, indices=None):
     return params, grads, moms, [shapes[i] for i in idx]
 
 
+VOCAB = 32768  # the tokenizer's vocabulary size
+
+
+def adamw_shapes(name: str):
+    """The parameters a dN model sends to AdamW (the optimizer split): the token embedding and
+    the untied lm_head (vocab x d each), two scalar lambdas per layer, the 24-wide smear gate
+    and the backout lambda."""
+    depth = STACK_DEPTHS[name]
+    d = 64 * depth
+    return [(VOCAB, d), (VOCAB, d)] + [(1,)] * (2 * depth) + [(24,), (1,)]
+
+
+def make_adamw_set(name: str, device="cpu", seed: int = 0):
+    """(params, grads, exp_avg, exp_avg_sq, shapes) for the AdamW parameters of a dN model:
+    p ~ N(0, 0.02^2), g ~ N(0, 1e-3^2), exp_avg ~ N(0, 1e-3^2), exp_avg_sq = N(0, 1e-3^2)^2."""
+    shapes = adamw_shapes(name)
+    tag = name + "_adamw"
+    ps = [_normal(s, 0.02, device, tensor_seed(seed, tag, i, "p")) for i, s in enumerate(shapes)]
+    gs = [_normal(s, 1e-3, device, tensor_seed(seed, tag, i, "g")) for i, s in enumerate(shapes)]
+    ms = [_normal(s, 1e-3, device, tensor_seed(seed, tag, i, "m")) for i, s in enumerate(shapes)]
+    vs = [_normal(s, 1e-3, device, tensor_seed(seed, tag, i, "s")) ** 2 for i, s in enumerate(shapes)]
+    return ps, gs, ms, vs, shapes
+
+
 def make_custom(shapes, device="cpu", seed: int = 0, tag: str = "custom"):
     """Stack-style inputs for an arbitrary list of shapes (tests of edge cases)."""
     params = [make_param(tag, i, s, device, seed) for i, s in enumerate(shapes)]
