@@ -65,6 +65,12 @@ def bind(lib):
     lib.oracle_muon_matrix.restype = ctypes.c_int
     lib.oracle_frobenius.argtypes = [ctypes.c_long, f64p]
     lib.oracle_frobenius.restype = ctypes.c_double
+    lib.oracle_normuon_scale.argtypes = [ctypes.c_int, ctypes.c_int, f64p, f32p, ctypes.c_double, ctypes.c_double]
+    lib.oracle_normuon_scale.restype = None
+    lib.oracle_normuon_matrix.argtypes = [ctypes.c_int, ctypes.c_int, f32p, f32p, f32p, ctypes.c_double,
+                                          ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, f64p,
+                                          ctypes.c_double, f32p, ctypes.c_double, ctypes.c_double, f32p, f32p, f64p]
+    lib.oracle_normuon_matrix.restype = ctypes.c_int
     lib.oracle_adamw.argtypes = [ctypes.c_long, f32p, f32p, f32p, f32p, ctypes.c_double, ctypes.c_double,
                                  ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int]
     lib.oracle_adamw.restype = None
@@ -173,3 +179,37 @@ def adamw(p, g, m, v, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, st
     _load().oracle_adamw(p.size, p.reshape(-1), g.reshape(-1), m.reshape(-1), v.reshape(-1), float(lr),
                          float(beta1), float(beta2), float(eps), float(weight_decay), int(step))
     return p, m, v
+
+
+NORMUON_BETA2 = 0.95
+NORMUON_EPS = 1e-10
+
+
+def normuon_scale(O, V, beta2=NORMUON_BETA2, eps=NORMUON_EPS):
+    """NorMuon-scaled copy of O (stored r x c) and the updated per-row state V (float32)."""
+    O = np.array(O, dtype=np.float64, order="C", copy=True)
+    V = np.array(V, dtype=np.float32, order="C", copy=True).reshape(-1)
+    r, c = O.shape
+    if V.size != r:
+        raise ValueError("V holds one value per stored row")
+    _load().oracle_normuon_scale(r, c, O, V, float(beta2), float(eps))
+    return O, V
+
+
+def normuon_matrix(p, g, m, V, lr, beta, nesterov=True, ns_steps=None, coeffs=DEFAULT_COEFFS, eps=DEFAULT_EPS,
+                   mode=0, beta2=NORMUON_BETA2, eps2=NORMUON_EPS):
+    """One Muon step with NorMuon scaling: returns (p', m', V', O')."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    m = np.ascontiguousarray(m, dtype=np.float32)
+    V = np.array(V, dtype=np.float32, order="C", copy=True).reshape(-1)
+    r, cc = p.shape
+    c, K = _coeffs(coeffs, ns_steps)
+    p_out = np.empty_like(p)
+    m_out = np.empty_like(m)
+    O = np.empty((r, cc), dtype=np.float64)
+    rc = _load().oracle_normuon_matrix(r, cc, p, g, m, float(lr), float(beta), int(bool(nesterov)), int(mode), K,
+                                       c, float(eps), V, float(beta2), float(eps2), p_out, m_out, O)
+    if rc != 0:
+        raise MemoryError("oracle allocation failed")
+    return p_out, m_out, V, O

@@ -228,3 +228,76 @@ void oracle_adamw(long n_elem, float* p, const float* g, float* m, float* v, dou
         v[e] = (float)vd;
     }
 }
+
+/*
+ * NorMuon variance scaling of an orthogonalised update O (stored r x c layout),
+ * as the apidog.com page's section "2. Pengoptimal Muon" (paragraph "Reduksi
+ * Varians NorMuon") and the dev.to page's "NorMuon variance scaling" sketch
+ * it: after orthogonalisation the update is normalised per neuron.  The
+ * sketch leaves red_dim, the second-moment state, step_size and v_norm_new
+ * undefined; the reading taken here:
+ *   a neuron is a stored row (an output unit): v_mean_i = mean_j O_ij^2
+ *   V_i   <- beta2 V_i + (1 - beta2) v_mean_i      (state across steps, float)
+ *   step_i = 1 / sqrt(V_i + eps)
+ *   v_norm     = sqrt(sum_i v_mean_i)
+ *   v_norm_new = sqrt(sum_i v_mean_i step_i^2)     (the same statistic of O * step)
+ *   O'_ij = O_ij step_i v_norm / max(v_norm_new, 1e-10)
+ * which keeps ||O'||_F = ||O||_F.  V is rounded to float where it is stored.
+ * O is overwritten by O'.  All sums in index order.
+ */
+void oracle_normuon_scale(int r, int c, double* O, float* V, double beta2, double eps) {
+    double* vm = (double*)malloc(sizeof(double) * (size_t)r);
+    double* st = (double*)malloc(sizeof(double) * (size_t)r);
+    if (!vm || !st) {
+        free(vm);
+        free(st);
+        return;
+    }
+    double s_old = 0.0, s_new = 0.0;
+    for (int i = 0; i < r; ++i) {
+        double s = 0.0;
+        for (int j = 0; j < c; ++j) s += O[(size_t)i * c + j] * O[(size_t)i * c + j];
+        vm[i] = s / (double)c;
+        const double Vn = beta2 * (double)V[i] + (1.0 - beta2) * vm[i];
+        V[i] = (float)Vn;
+        st[i] = 1.0 / sqrt(Vn + eps);
+        s_old += vm[i];
+        s_new += vm[i] * st[i] * st[i];
+    }
+    const double v_norm = sqrt(s_old);
+    const double v_norm_new = sqrt(s_new);
+    const double ratio = v_norm / (v_norm_new > 1e-10 ? v_norm_new : 1e-10);
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < c; ++j) O[(size_t)i * c + j] *= st[i] * ratio;
+    free(vm);
+    free(st);
+}
+
+/*
+ * One Muon step with NorMuon scaling: as oracle_muon_matrix, with O replaced
+ * by its NorMuon-scaled O' before the update p' = p - lr sqrt(max(1, r/c)) O'.
+ * V (r floats) is the per-row second-moment state, updated in place.
+ */
+int oracle_normuon_matrix(int r, int c, const float* p, const float* g, const float* m, double lr, double beta,
+                          int nesterov, int mode, int K, const double* coeffs, double eps, float* V,
+                          double beta2, double eps2, float* p_out, float* m_out, double* O_out) {
+    const size_t rc = (size_t)r * c;
+    double* u = (double*)malloc(sizeof(double) * rc);
+    double* O = O_out ? O_out : (double*)malloc(sizeof(double) * rc);
+    if (!u || !O) {
+        free(u);
+        if (!O_out) free(O);
+        return -1;
+    }
+    oracle_momentum((long)rc, g, m, beta, nesterov, mode, m_out, u);
+    int rcode = oracle_orthogonalize(r, c, u, K, coeffs, eps, O);
+    if (rcode == 0) {
+        oracle_normuon_scale(r, c, O, V, beta2, eps2);
+        const double ratio = (double)r / (double)c;
+        const double scale = lr * sqrt(ratio > 1.0 ? ratio : 1.0);
+        for (size_t e = 0; e < rc; ++e) p_out[e] = (float)((double)p[e] - scale * O[e]);
+    }
+    free(u);
+    if (!O_out) free(O);
+    return rcode;
+}
