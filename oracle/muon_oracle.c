@@ -172,6 +172,12 @@ int oracle_orthogonalize(int r, int c, const double* u, int K, const double* coe
     return 0;
 }
 
+/* Update scale of a stored r x c matrix: sqrt(max(1, r / c)). */
+static double oracle_aspect_scale(int r, int c) {
+    const double ratio = (double)r / (double)c;
+    return sqrt(ratio > 1.0 ? ratio : 1.0);
+}
+
 /*
  * One full Muon step on one stored r x c matrix.
  * Inputs p, g, m (float, r x c).  Outputs: p_out (p', float), m_out (m',
@@ -192,8 +198,7 @@ int oracle_muon_matrix(int r, int c, const float* p, const float* g, const float
     oracle_momentum((long)rc, g, m, beta, nesterov, mode, m_out, u);
     int rcode = oracle_orthogonalize(r, c, u, K, coeffs, eps, O);
     if (rcode == 0) {
-        const double ratio = (double)r / (double)c;
-        const double scale = lr * sqrt(ratio > 1.0 ? ratio : 1.0);
+        const double scale = lr * oracle_aspect_scale(r, c);
         for (size_t e = 0; e < rc; ++e) p_out[e] = (float)((double)p[e] - scale * O[e]);
     }
     free(u);
@@ -293,8 +298,7 @@ int oracle_normuon_matrix(int r, int c, const float* p, const float* g, const fl
     int rcode = oracle_orthogonalize(r, c, u, K, coeffs, eps, O);
     if (rcode == 0) {
         oracle_normuon_scale(r, c, O, V, beta2, eps2);
-        const double ratio = (double)r / (double)c;
-        const double scale = lr * sqrt(ratio > 1.0 ? ratio : 1.0);
+        const double scale = lr * oracle_aspect_scale(r, c);
         for (size_t e = 0; e < rc; ++e) p_out[e] = (float)((double)p[e] - scale * O[e]);
     }
     free(u);
