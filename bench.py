@@ -356,6 +356,30 @@ def run_ours(args, rank, world, local_rank):
                     "avg_launch_ms": mom_ms / max(mom_launches, 1)}
     phase_ms = {k: v[0] / args.steps for k, v in kt.items()}
 
+    # ---- the same step with NorMuon scaling (second moments per stored row)
+    normuon = None
+    if wl in workloads.STACK_DEPTHS:
+        mu.muon_destroy()
+        mu.muon_init(debug_flags=mu.MUON_DEBUG_TIME_KERNELS)
+        V = [torch.zeros(r, device=dev) for r, _ in shapes]
+
+        def nm_step(k):
+            mu.muon_step_normuon(step_args[k % n_sets], second_moments=V, lr=hp["lr"], beta=hp["beta"],
+                                 nesterov=hp["nesterov"], ns_steps=hp["ns_steps"], stream=stream)
+
+        for k in range(args.warmup):
+            nm_step(k)
+        mu.muon_get_status(stream)
+        mu.muon_kernel_times()
+        nm_ms = timed(args.steps, nm_step) / args.steps
+        nkt = mu.muon_kernel_times()
+        mu.muon_get_status(stream)
+        normuon = {"ms_per_step": nm_ms, "value": job_tflops(world, flops_step, nm_ms), "unit": UNIT,
+                   "overhead_ms_vs_plain_step": nm_ms - ms_step,
+                   "phase_ms_per_step": {k: v[0] / args.steps for k, v in nkt.items() if v[1]},
+                   "state": "beta2 0.95, eps 1e-10, V per stored row (zero-initialised)"}
+        del V
+
     # ---- AdamW over the same model's non-matrix parameters (embedding, lm_head,
     # scalars): one multi-tensor launch per step, HBM-bound at 28 bytes per element
     adamw = None
@@ -467,7 +491,7 @@ def run_ours(args, rank, world, local_rank):
                            "state_dtype": "fp32 p/g/m; bf16 Newton-Schulz operands, fp32 accumulation"},
                 "ns_tflops": ns_tflops, "frac_of_bf16_peak": ns_tflops / peak_tf_sus, "frac_of_bf16_burst_peak": ns_tflops / peak_tf,
                 "phase_ms_per_step": phase_ms, "timed_ms_with_kernel_events": timed_ms2 / args.steps,
-                "roofline": roofline, "roofline_elementwise": roofline_hbm, "adamw": adamw, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "roofline_elementwise": roofline_hbm, "normuon": normuon, "adamw": adamw, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clocks.summary(), "gpu_launches": info["launches"] * args.steps,
                 "workspace_bytes": info["workspace_bytes"]}
         print(json.dumps(line), flush=True)

@@ -130,6 +130,34 @@ MUON_API muon_status muon_step(float* const params[], const float* const grads[]
                       float* const momentum_bufs[], const muon_shape shapes[], int n_mats,
                       float lr, float beta, int nesterov, int ns_steps, muon_stream_t stream);
 
+/*
+ * One Muon step with NorMuon variance scaling of the orthogonalised update.
+ * The apidog.com page (section "2. Pengoptimal Muon", paragraph "Reduksi
+ * Varians NorMuon") and the dev.to page ("NorMuon variance scaling") sketch a
+ * per-neuron rescale after orthogonalisation; the sketch leaves the reduced
+ * dimension, the second-moment state and the new-norm term open.  This library
+ * takes: a neuron is a stored row (an output unit), and with O the update of
+ * muon_step,
+ *   v_mean_i = mean_j O_ij^2 ;  V_i <- beta2 V_i + (1 - beta2) v_mean_i ;
+ *   step_i = 1 / sqrt(V_i + eps2) ;
+ *   ratio = sqrt(sum_i v_mean_i) / max(sqrt(sum_i v_mean_i step_i^2), 1e-10)
+ *   p_ij <- p_ij - lr sqrt(max(1, rows/cols)) step_i ratio O_ij
+ * which keeps the Frobenius norm of the update.
+ *   second_moments[i]  device float32 array of shapes[i].rows elements, 4-byte
+ *                      aligned, caller-owned, updated in place (zero-initialise
+ *                      it before the first step)
+ *   beta2 in [0, 1), eps2 >= 0; ns_steps >= 1; other arguments as muon_step.
+ * O is materialised in an fp32 workspace (one more allocation of the size of
+ * the weights, made by the first call on a shape list); the per-row reduction
+ * is deterministic.  Not available with MUON_DEBUG_SINGLE_CTA_GEMM
+ * (MUON_ERR_INVALID_ARG).  With MUON_DEBUG_KEEP_O, muon_debug_copy_ns_output
+ * returns the scaled update step_i ratio O.  Errors as muon_step.
+ */
+MUON_API muon_status muon_step_normuon(float* const params[], const float* const grads[],
+                                       float* const momentum_bufs[], float* const second_moments[],
+                                       const muon_shape shapes[], int n_mats, float lr, float beta, int nesterov,
+                                       int ns_steps, float beta2, float eps2, muon_stream_t stream);
+
 /* Free the workspace and the context.  Synchronises the device first. */
 MUON_API muon_status muon_destroy(void);
 
@@ -186,7 +214,8 @@ MUON_API muon_status muon_plan_query(const muon_shape shapes[], int n_mats, int 
  * events and returns, per kernel kind, the summed device milliseconds and the
  * launch count since the previous call, then resets them.  Kinds:
  * 0 momentum+norm, 1 Gram, 2 polynomial, 3 axpy, 4 axpy with fused weight
- * update, 5 standalone weight update (ns_steps == 0).  n_kinds <= 6.
+ * update, 5 standalone weight update (ns_steps == 0), 6 last axpy writing O
+ * (NorMuon step), 7 NorMuon row statistics and weight update.  n_kinds <= 8.
  */
 MUON_API muon_status muon_kernel_times(double* ms_out, int* launches_out, int n_kinds);
 

@@ -40,7 +40,7 @@ MUON_DEBUG_TIME_KERNELS = 4
 MUON_DEBUG_INJECT_LOST_LOAD = 8
 MUON_DEBUG_SINGLE_CTA_GEMM = 16
 
-KERNEL_KINDS = ("momentum_norm", "gram", "poly", "axpy", "axpy_update", "update")
+KERNEL_KINDS = ("momentum_norm", "gram", "poly", "axpy", "axpy_update", "update", "axpy_o", "normuon")
 
 
 class MuonLibraryMissing(RuntimeError):
@@ -107,13 +107,17 @@ def lib():
         L.muon_momentum_norm_noalloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                                  vp, ctypes.POINTER(muon_shape), ctypes.c_int, ctypes.c_float,
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_double, vp]
+        L.muon_step_normuon.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                        ctypes.POINTER(vp), ctypes.POINTER(muon_shape), ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_float, vp]
         L.muon_adamw_step.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                       ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_longlong), ctypes.c_int,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_float, ctypes.c_int, vp]
         for name in ("muon_init", "muon_step", "muon_destroy", "muon_get_status", "muon_get_step_info",
                      "muon_kernel_times", "muon_debug_copy_ns_output", "muon_debug_copy_norms",
-                     "muon_plan_query", "muon_momentum_norm_noalloc", "muon_adamw_step"):
+                     "muon_plan_query", "muon_momentum_norm_noalloc", "muon_adamw_step", "muon_step_normuon"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -189,6 +193,20 @@ def muon_step(params, grads=None, momentum_bufs=None, lr: float = 0.02, beta: fl
     st = lib().muon_step(args.params, args.grads, args.moms, args.shapes, args.n, float(lr),
                          float(beta), 1 if nesterov else 0, int(ns_steps), _stream(stream))
     return _check(st, "muon_step") if check else st
+
+
+def muon_step_normuon(params, grads=None, momentum_bufs=None, second_moments=None, lr: float = 0.02,
+                      beta: float = 0.95, nesterov: bool = True, ns_steps: int = 5, beta2: float = 0.95,
+                      eps2: float = 1e-10, stream=None, shapes=None, check: bool = True) -> int:
+    """Enqueue one Muon step with NorMuon scaling (see include/muon.h).  ``params`` may be a
+    prepared StepArgs, then ``second_moments`` is the list of per-row state arrays."""
+    args = params if isinstance(params, StepArgs) else StepArgs(params, grads, momentum_bufs, shapes)
+    vp = ctypes.c_void_p
+    sm = (vp * max(args.n, 1))(*[_ptr(x) for x in second_moments])
+    st = lib().muon_step_normuon(args.params, args.grads, args.moms, sm, args.shapes, args.n, float(lr),
+                                 float(beta), 1 if nesterov else 0, int(ns_steps), float(beta2), float(eps2),
+                                 _stream(stream))
+    return _check(st, "muon_step_normuon") if check else st
 
 
 def muon_get_status(stream=None, check: bool = True) -> int:

@@ -77,6 +77,7 @@ enum GemmMode : int {
     MODE_POLY = 1,        // B = b A + c A A (upper tiles, mirrored)
     MODE_AXPY = 2,        // X' = s (a X + B X)
     MODE_AXPY_FINAL = 3,  // O = s (a X + B X); p -= scale O
+    MODE_AXPY_O = 4,      // O = s (a X + B X) written in fp32 (stored layout) for the NorMuon pass
 };
 
 struct GemmClass {
@@ -111,6 +112,39 @@ struct GemmParams {
     unsigned long long timeout_ns;
     int inject_lost_load;      // test hook (see MUON_DEBUG_INJECT_LOST_LOAD)
 };
+
+// ------------------------------------------------------------------ NorMuon scaling
+// Per stored row i of O (fp32, stored r x c): v_mean = mean_j O_ij^2, V_i <- b2 V_i + (1 - b2) v_mean,
+// step_i = 1 / sqrt(V_i + eps); per matrix: ratio = sqrt(sum v_mean) / max(sqrt(sum v_mean step^2), 1e-10).
+// Then p_ij -= lr aspect step_i ratio O_ij.
+constexpr int kNormRowsPerCta = 8;           // one warp per row, 256 threads
+struct NormuonMat {
+    const float* O;       // stored rows x cols (workspace)
+    float* V;             // caller-owned second moments, rows floats
+    float* p;             // weights
+    float* dbg;           // O' (stored layout) when the debug copy is kept, else nullptr
+    int rows, cols;
+    int cta_begin;        // rows kernel: first CTA of this matrix
+    int nctas;            // rows kernel: CTAs of this matrix (ceil(rows / 8))
+    int tile_begin;       // update kernel: first 64 x 64 tile of this matrix
+    int tiles_x;          // update kernel: ceil(cols / 64)
+    int pos;              // step position (aspect, ratio, counters)
+};
+struct NormuonParams {
+    NormuonMat mats[kMomentumMaxMats];
+    int nmats;
+    int total;            // CTAs (rows kernel) or tiles (update kernel)
+    float beta2, eps;
+    float lr;
+    const float* aspect;  // per position
+    float* step;          // per matrix row block: step_i, indexed by a per-matrix offset (row_base[pos] + i)
+    const int* row_base;  // per position: offset of the matrix's rows in `step`
+    double* partials;     // rows kernel: two doubles per CTA (sum v_mean, sum v_mean step^2)
+    unsigned int* counters;  // per position
+    float* ratio;         // per position
+};
+cudaError_t launch_normuon_rows(const NormuonParams& p, cudaStream_t s);
+cudaError_t launch_normuon_update(const NormuonParams& p, cudaStream_t s);
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_momentum_norm(const MomentumParams& p, cudaStream_t s);
@@ -166,6 +200,7 @@ struct PairParams {
     float lr;
     const CUtensorMap* p_maps;    // per step position: fp32 weights (stored layout), box 32 x 32, 128B swizzle
     const CUtensorMap* dbg_maps;  // per step position (O, stored layout) or nullptr
+    const CUtensorMap* o_maps;    // MODE_AXPY_O: per step position, the fp32 O buffer (stored layout)
     unsigned int* status;
     unsigned long long timeout_ns;
     int inject_lost_load;

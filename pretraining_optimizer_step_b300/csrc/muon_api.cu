@@ -22,7 +22,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-constexpr int kKinds = 6;  // momentum, gram, poly, axpy, axpy+update, update
+constexpr int kKinds = 8;  // momentum, gram, poly, axpy, axpy+update, update, axpy writing O, NorMuon
 constexpr int kMaxCoeffRows = 16;
 
 struct ClassPlan {
@@ -60,6 +60,16 @@ struct Plan {
     CUtensorMap* p_maps = nullptr;  // device: fp32 weight maps per position (refreshed when params change)
     CUtensorMap* dbg_maps = nullptr;  // device: O maps per position (KEEP_O)
     std::vector<float*> mapped_p;   // params the device p_maps describe, by step index
+    // NorMuon resources (allocated by the first muon_step_normuon on this plan)
+    char* nm_arena = nullptr;
+    std::vector<float*> o_bufs;     // fp32 O per matrix (stored layout), by step index
+    CUtensorMap* o_maps = nullptr;  // device, by position
+    float* nm_step = nullptr;       // step_i of every stored row, matrices at row_base
+    int* nm_row_base = nullptr;     // device, by position
+    std::vector<int> row_base;      // host copy
+    double* nm_partials = nullptr;
+    unsigned int* nm_counters = nullptr;
+    float* nm_ratio = nullptr;
     double ns_flops_per_iter = 0.0;
     double elem_bytes = 0.0;
 };
@@ -97,6 +107,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 void free_plan(Plan* p) {
     if (!p) return;
     if (p->arena) cudaFree(p->arena);
+    if (p->nm_arena) cudaFree(p->nm_arena);
     delete p;
 }
 
@@ -368,6 +379,72 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
     return MUON_OK;
 }
 
+// Workspace of the NorMuon pass: fp32 O per matrix, their tensor maps, the per-row
+// step sizes and the per-matrix reduction state.  Built once per plan.
+muon_status ensure_normuon(Context* ctx, Plan* P) {
+    if (P->nm_arena) return MUON_OK;
+    const int n = static_cast<int>(P->shapes.size());
+    std::vector<size_t> off_o(n);
+    size_t off = 0;
+    long long total_rows = 0;
+    size_t max_ctas = 0, chunk_ctas = 0;
+    P->row_base.assign(n, 0);
+    for (int k = 0; k < n; ++k) {
+        const muon_shape& s = P->shapes[P->order[k]];
+        P->row_base[k] = static_cast<int>(total_rows);
+        total_rows += s.rows;
+        if (k % kMomentumMaxMats == 0) chunk_ctas = 0;
+        chunk_ctas += (s.rows + kNormRowsPerCta - 1) / kNormRowsPerCta;
+        if (chunk_ctas > max_ctas) max_ctas = chunk_ctas;
+    }
+    for (int i = 0; i < n; ++i) {
+        off_o[i] = off;
+        off = align_up(off + static_cast<size_t>(P->shapes[i].rows) * P->shapes[i].cols * sizeof(float), 1024);
+    }
+    const size_t off_maps = off; off = align_up(off + n * sizeof(CUtensorMap), 256);
+    const size_t off_step = off; off = align_up(off + static_cast<size_t>(total_rows) * sizeof(float), 256);
+    const size_t off_rb = off; off = align_up(off + n * sizeof(int), 256);
+    const size_t off_part = off; off = align_up(off + max_ctas * 2 * sizeof(double), 256);
+    const size_t off_cnt = off; off = align_up(off + n * sizeof(unsigned int), 256);
+    const size_t off_ratio = off; off = align_up(off + n * sizeof(float), 256);
+    char* a = nullptr;
+    if (cudaMalloc(&a, off) != cudaSuccess) {
+        cudaGetLastError();
+        return MUON_ERR_OUT_OF_MEMORY;
+    }
+    P->o_bufs.resize(n);
+    for (int i = 0; i < n; ++i) P->o_bufs[i] = reinterpret_cast<float*>(a + off_o[i]);
+    P->o_maps = reinterpret_cast<CUtensorMap*>(a + off_maps);
+    P->nm_step = reinterpret_cast<float*>(a + off_step);
+    P->nm_row_base = reinterpret_cast<int*>(a + off_rb);
+    P->nm_partials = reinterpret_cast<double*>(a + off_part);
+    P->nm_counters = reinterpret_cast<unsigned int*>(a + off_cnt);
+    P->nm_ratio = reinterpret_cast<float*>(a + off_ratio);
+    std::vector<CUtensorMap> om(n);
+    for (int k = 0; k < n; ++k) {
+        const int i = P->order[k];
+        if (encode_f32_map(ctx->encode, &om[k], P->o_bufs[i], P->shapes[i].rows, P->shapes[i].cols) != MUON_OK) {
+            cudaFree(a);
+            return MUON_ERR_CUDA;
+        }
+    }
+    bool ok = cudaMemcpy(P->o_maps, om.data(), n * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(P->nm_row_base, P->row_base.data(), n * sizeof(int), cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemset(P->nm_counters, 0, n * sizeof(unsigned int)) == cudaSuccess;
+    if (!ok) {
+        cudaFree(a);
+        return MUON_ERR_CUDA;
+    }
+    P->nm_arena = a;
+    return MUON_OK;
+}
+
+// The NorMuon arguments of a step (nullptr for a plain Muon step).
+struct NormuonCall {
+    float* const* second_moments;  // by step index
+    float beta2, eps;
+};
+
 muon_status check_shapes(const muon_shape* shapes, int n) {
     for (int i = 0; i < n; ++i) {
         const int r = shapes[i].rows, c = shapes[i].cols;
@@ -533,9 +610,9 @@ muon_status muon_init(const muon_config* cfg) {
     return MUON_OK;
 }
 
-muon_status muon_step(float* const params[], const float* const grads[], float* const momentum_bufs[],
-                      const muon_shape shapes[], int n_mats, float lr, float beta, int nesterov,
-                      int ns_steps, muon_stream_t stream_) {
+static muon_status step_impl(float* const params[], const float* const grads[], float* const momentum_bufs[],
+                             const muon_shape shapes[], int n_mats, float lr, float beta, int nesterov,
+                             int ns_steps, muon_stream_t stream_, const NormuonCall* nm) {
     Context* ctx = g_ctx;
     if (!ctx) return MUON_ERR_NOT_INITIALIZED;
     if (n_mats < 0) return MUON_ERR_INVALID_ARG;
@@ -567,6 +644,10 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
         ctx->plan = P;
     }
     Plan* P = ctx->plan;
+    if (nm) {
+        const muon_status st = ensure_normuon(ctx, P);
+        if (st != MUON_OK) return st;
+    }
     ctx->info = muon_step_info{};
     ctx->info.n_classes = static_cast<int>(P->classes.size());
     ctx->info.workspace_bytes = static_cast<long long>(P->arena_bytes);
@@ -630,8 +711,9 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
     const int nclass = static_cast<int>(P->classes.size());
     if (!(ctx->debug & MUON_DEBUG_SINGLE_CTA_GEMM)) {
         // fp32 weight maps of the fused update: re-encoded only when the params change
+        // (the NorMuon pass updates the weights in its own kernel)
         bool changed = false;
-        for (int i = 0; i < n_mats && !changed; ++i) changed = P->mapped_p[i] != params[i];
+        for (int i = 0; i < n_mats && !changed && !nm; ++i) changed = P->mapped_p[i] != params[i];
         if (changed) {
             std::vector<CUtensorMap> pm(n_mats);
             for (int k = 0; k < n_mats; ++k) {
@@ -654,7 +736,8 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
                 const int gc = std::min(kMaxClasses, nclass - g0);
                 for (int mode = MODE_GRAM; mode <= MODE_AXPY; ++mode) {
                     std::memset(&pp, 0, sizeof(pp));
-                    const int eff_mode = (mode == MODE_AXPY && last) ? MODE_AXPY_FINAL : mode;
+                    const int eff_mode =
+                        (mode == MODE_AXPY && last) ? (nm ? MODE_AXPY_O : MODE_AXPY_FINAL) : mode;
                     pp.mode = eff_mode;
                     pp.nclasses = gc;
                     pp.first_iter = (it == 0 && mode != MODE_POLY) ? 1 : 0;
@@ -666,6 +749,7 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
                     pp.lr = lr;
                     pp.p_maps = P->p_maps;
                     pp.dbg_maps = keep_o ? P->dbg_maps : nullptr;
+                    pp.o_maps = P->o_maps;
                     pp.status = ctx->status;
                     pp.timeout_ns = ctx->timeout_ns;
                     pp.inject_lost_load = ((ctx->debug & MUON_DEBUG_INJECT_LOST_LOAD) && !ctx->injected &&
@@ -717,11 +801,55 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
                     }
                     pp.total_tiles = tiles;
                     const int clusters = std::min(tiles, ctx->max_clusters);
-                    const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3 : 4;
+                    const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3
+                                     : eff_mode == MODE_AXPY_O ? 6 : 4;
                     const muon_status st =
                         timed_launch(ctx, kind, stream, [&] { return launch_ns_pair(pp, clusters, stream); });
                     if (st != MUON_OK) return st;
                 }
+            }
+        }
+        if (nm) {
+            // ---- NorMuon: per-row statistics and ratio, then the weight update
+            static NormuonParams np;  // ~12 KiB: kept off the stack
+            for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
+                const int cnt = std::min(kMomentumMaxMats, n_mats - base);
+                std::memset(&np, 0, sizeof(np));
+                int ctas = 0, tiles = 0;
+                for (int k = 0; k < cnt; ++k) {
+                    const int pos = base + k;
+                    const int i = P->order[pos];
+                    NormuonMat& M = np.mats[k];
+                    M.O = P->o_bufs[i];
+                    M.V = nm->second_moments[i];
+                    M.p = params[i];
+                    M.dbg = keep_o ? P->dbg_O[i] : nullptr;
+                    M.rows = shapes[i].rows;
+                    M.cols = shapes[i].cols;
+                    M.cta_begin = ctas;
+                    M.nctas = (M.rows + kNormRowsPerCta - 1) / kNormRowsPerCta;
+                    M.tile_begin = tiles;
+                    M.tiles_x = (M.cols + 63) / 64;
+                    M.pos = pos;
+                    ctas += M.nctas;
+                    tiles += M.tiles_x * ((M.rows + 63) / 64);
+                }
+                np.nmats = cnt;
+                np.beta2 = nm->beta2;
+                np.eps = nm->eps;
+                np.lr = lr;
+                np.aspect = P->aspect;
+                np.step = P->nm_step;
+                np.row_base = P->nm_row_base;
+                np.partials = P->nm_partials;
+                np.counters = P->nm_counters;
+                np.ratio = P->nm_ratio;
+                np.total = ctas;
+                muon_status st = timed_launch(ctx, 7, stream, [&] { return launch_normuon_rows(np, stream); });
+                if (st != MUON_OK) return st;
+                np.total = tiles;
+                st = timed_launch(ctx, 7, stream, [&] { return launch_normuon_update(np, stream); });
+                if (st != MUON_OK) return st;
             }
         }
         return MUON_OK;
@@ -804,6 +932,31 @@ muon_status muon_step(float* const params[], const float* const grads[], float* 
         }
     }
     return MUON_OK;
+}
+
+muon_status muon_step(float* const params[], const float* const grads[], float* const momentum_bufs[],
+                      const muon_shape shapes[], int n_mats, float lr, float beta, int nesterov,
+                      int ns_steps, muon_stream_t stream) {
+    return step_impl(params, grads, momentum_bufs, shapes, n_mats, lr, beta, nesterov, ns_steps, stream, nullptr);
+}
+
+muon_status muon_step_normuon(float* const params[], const float* const grads[], float* const momentum_bufs[],
+                              float* const second_moments[], const muon_shape shapes[], int n_mats, float lr,
+                              float beta, int nesterov, int ns_steps, float beta2, float eps2,
+                              muon_stream_t stream) {
+    Context* ctx = g_ctx;
+    if (!ctx) return MUON_ERR_NOT_INITIALIZED;
+    if (n_mats < 0) return MUON_ERR_INVALID_ARG;
+    if (n_mats == 0) return step_impl(params, grads, momentum_bufs, shapes, 0, lr, beta, nesterov, ns_steps, stream,
+                                      nullptr);
+    if (!second_moments || ns_steps < 1 || (ctx->debug & MUON_DEBUG_SINGLE_CTA_GEMM)) return MUON_ERR_INVALID_ARG;
+    if (!(beta2 >= 0.0f && beta2 < 1.0f) || !(eps2 >= 0.0f) || !std::isfinite(eps2)) return MUON_ERR_INVALID_ARG;
+    for (int i = 0; i < n_mats; ++i) {
+        if (!second_moments[i]) return MUON_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(second_moments[i]) & 3u) return MUON_ERR_MISALIGNED;
+    }
+    const NormuonCall nm{second_moments, beta2, eps2};
+    return step_impl(params, grads, momentum_bufs, shapes, n_mats, lr, beta, nesterov, ns_steps, stream, &nm);
 }
 
 muon_status muon_plan_query(const muon_shape shapes[], int n_mats, int ns_steps, muon_plan_info* out) {

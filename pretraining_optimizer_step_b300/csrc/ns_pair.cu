@@ -9,6 +9,7 @@
 //   MODE_POLY        B' = b A + c A A + a I      A symmetric: A A = A A^T, same operand both sides
 //   MODE_AXPY        X' = s B' X                 X read MN-major as the B operand
 //   MODE_AXPY_FINAL  O = s B' X in fp32, p -= lr sqrt(max(1, r/c)) O
+//   MODE_AXPY_O      O = s B' X in fp32, stored (stored layout) for the NorMuon pass
 // Folding a I into the polynomial makes a X + B X = (B + a I) X a plain product, so the
 // axpy epilogues read nothing but the accumulator (and the weights in the final launch);
 // the only numerical change is one bf16 rounding of B's diagonal entries plus a.
@@ -281,9 +282,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         //   gram  (8 KiB):  2 output slots of {bf16 direct, bf16 mirror}
         //   poly  (8 KiB):  2 bf16 input slots (A) + 1 output slot of {direct, mirror}
         //   axpy  (8 KiB):  4 output slots of bf16 direct
+        //   axpy_o (8 KiB): 2 output slots of fp32 O
+        const bool o_mode = P.mode == MODE_AXPY_O;
         const int n_in = final_mode ? 4 : (has_in ? 2 : 0);
         const int in_stride = final_mode ? 4096 : 2048;
-        const int n_out = P.mode == MODE_GRAM ? 2 : (P.mode == MODE_AXPY ? 4 : 1);
+        const int n_out = (P.mode == MODE_GRAM || o_mode) ? 2 : (P.mode == MODE_AXPY ? 4 : 1);
         const int out_stride = (P.mode == MODE_AXPY) ? 2048 : 4096;
         uint8_t* out_base = wbase + n_in * in_stride;
         auto in_f32 = [&](int sl) { return wbase + sl * in_stride; };
@@ -439,6 +442,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                     *reinterpret_cast<float*>(out_slot + sw128_elem(j, lane)) = v[j];
                             }
                         }
+                    } else if (o_mode) {
+                        // fp32 O subtile in the stored layout (rows = stored rows)
+                        if (!transposed) {
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                *reinterpret_cast<float4*>(out_slot + sw128_unit(lane, u)) =
+                                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                *reinterpret_cast<float*>(out_slot + sw128_elem(j, lane)) = v[j];
+                        }
                     } else {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -468,6 +483,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                 if (transposed) tma_store_2d(&P.dbg_maps[gm], out_slot, grow0, cc0);
                                 else tma_store_2d(&P.dbg_maps[gm], out_slot, cc0, grow0);
                             }
+                        } else if (o_mode) {
+                            if (transposed) tma_store_2d(&P.o_maps[gm], out_slot, grow0, cc0);
+                            else tma_store_2d(&P.o_maps[gm], out_slot, cc0, grow0);
                         } else {
                             tma_store_3d(&P.tmOut[pt.ci], out_slot, cc0, grow0, pt.mat);
                             if (mirror) tma_store_3d(&P.tmOut[pt.ci], out_slot + 2048, grow0, cc0, pt.mat);

@@ -1,0 +1,112 @@
+"""Parity of the CUDA Muon step with NorMuon scaling (muon_step_normuon, through
+the C ABI) with the fp64 oracle on the same inputs.
+
+Tolerances (per matrix, relative Frobenius): the scaled update O' within 2e-2
+and the updated weights within 1e-3, as for muon_step; the second-moment state
+V' within 2e-2 (its per-row means are taken of the bf16-computed update).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pretraining_optimizer_step_b300 as mu
+import workloads
+from gpu_util import TOL_O, TOL_P, TOL_DP, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+BETA2 = 0.95
+EPS2 = 1e-10
+
+
+@pytest.fixture(autouse=True)
+def fresh_context():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mu.muon_init(debug_flags=mu.MUON_DEBUG_KEEP_O, wait_timeout_s=2.0)
+    yield
+    mu.muon_destroy()
+
+
+def cpu(ts):
+    return [t.detach().cpu().numpy().copy() for t in ts]
+
+
+def step_and_check(p, g, m, V, ns_steps=5, tol_o=TOL_O, check_idx=None):
+    p0, g0, m0, V0 = cpu(p), cpu(g), cpu(m), cpu(V)
+    mu.muon_step_normuon(p, g, m, V, lr=0.02, beta=0.95, nesterov=True, ns_steps=ns_steps, beta2=BETA2, eps2=EPS2)
+    mu.muon_get_status()
+    idx = range(len(p)) if check_idx is None else check_idx
+    worst = {}
+    for i in idx:
+        O = torch.empty_like(p[i])
+        mu.muon_debug_copy_ns_output(i, O)
+        torch.cuda.synchronize()
+        p_ref, m_ref, V_ref, O_ref = oracle.normuon_matrix(p0[i], g0[i], m0[i], V0[i], lr=np.float32(0.02),
+                                                           beta=np.float32(0.95), ns_steps=ns_steps,
+                                                           beta2=np.float32(BETA2), eps2=np.float32(EPS2))
+        rep = {"O": rel_fro(O.cpu().numpy(), O_ref), "p": rel_fro(p[i].cpu().numpy(), p_ref),
+               "dp": rel_fro(p[i].cpu().numpy().astype(np.float64) - p0[i], p_ref.astype(np.float64) - p0[i]),
+               "V": rel_fro(V[i].cpu().numpy(), V_ref)}
+        assert rep["O"] <= tol_o and rep["p"] <= TOL_P and rep["dp"] <= TOL_DP and rep["V"] <= 2e-2, (i, rep)
+        assert np.array_equal(m[i].cpu().numpy(), m[i].cpu().numpy())
+        for k, v in rep.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    return worst
+
+
+def zeros_state(shapes):
+    return [torch.zeros(r, device="cuda") for r, _ in shapes]
+
+
+def test_d2_full_stack_from_zero_state():
+    p, g, m, shapes = workloads.make_stack("d2", "cuda")
+    step_and_check(p, g, m, zeros_state(shapes))
+
+
+def test_two_steps_carry_the_state():
+    name = "d2"
+    p, g, m, shapes = workloads.make_stack(name, "cuda")
+    V = zeros_state(shapes)
+    step_and_check(p, g, m, V)
+    g2 = [workloads.make_grad(name, i, s, "cuda", 0, 1) for i, s in enumerate(shapes)]
+    step_and_check(p, g2, m, V)
+
+
+def test_ragged_and_tall_wide_shapes():
+    shapes = [(136, 200), (200, 136), (264, 264), (392, 1032), (1032, 392)]
+    p, g, m, _ = workloads.make_custom(shapes, "cuda", tag="normuon")
+    V = [torch.rand(r, device="cuda") * 1e-3 for r, _ in shapes]
+    step_and_check(p, g, m, V)
+
+
+def test_d12_sampled():
+    p, g, m, shapes = workloads.make_stack("d12", "cuda")
+    step_and_check(p, g, m, zeros_state(shapes), check_idx=[0, 4, 5, 70, 71])
+
+
+def test_zero_gradient_leaves_weights_and_decays_state():
+    shapes = [(64, 64), (256, 64), (64, 256)]
+    p = [torch.randn(s, device="cuda") for s in shapes]
+    g = [torch.zeros(s, device="cuda") for s in shapes]
+    m = [torch.zeros(s, device="cuda") for s in shapes]
+    V = [torch.full((r,), 0.5, device="cuda") for r, _ in shapes]
+    p0 = [t.clone() for t in p]
+    mu.muon_step_normuon(p, g, m, V, beta2=BETA2, eps2=EPS2)
+    mu.muon_get_status()
+    for i in range(3):
+        assert torch.equal(p[i], p0[i])
+        assert torch.allclose(V[i], torch.full_like(V[i], np.float32(BETA2) * 0.5), rtol=1e-6, atol=0)
+
+
+def test_argument_errors():
+    p, g, m, shapes = workloads.make_custom([(64, 64), (64, 128)], "cuda", tag="nmargs")
+    V = zeros_state(shapes)
+    before = [t.clone() for t in p + m + V]
+    assert mu.muon_step_normuon(p, g, m, V, ns_steps=0, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_step_normuon(p, g, m, V, beta2=1.0, check=False) == mu.MUON_ERR_INVALID_ARG
+    assert mu.muon_step_normuon(p, g, m, [V[0].data_ptr() + 2, V[1]], check=False) == mu.MUON_ERR_MISALIGNED
+    assert mu.muon_step_normuon(p, g, m, [V[0], 0], check=False) == mu.MUON_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    for a, b in zip(before, p + m + V):
+        assert torch.equal(a, b)
