@@ -158,6 +158,20 @@ MUON_API muon_status muon_step_normuon(float* const params[], const float* const
                                        const muon_shape shapes[], int n_mats, float lr, float beta, int nesterov,
                                        int ns_steps, float beta2, float eps2, muon_stream_t stream);
 
+/*
+ * Ownership of the matrices of a step across `world` data-parallel ranks, for
+ * the ZeRO-2-style sharded step the pages describe (apidog.com section
+ * "2. Pengoptimal Muon", paragraph "Pelatihan Terdistribusi": reduce-scatter the
+ * gradients, each rank updates the matrices it owns, all-gather the weights).
+ * Host only (needs no device and no muon_init).  Matrices are assigned largest
+ * first, each to the rank with the least Newton-Schulz work so far (work per
+ * matrix: 3 m^2 n + m^3 with m <= n its sides; ties go to the lower rank), so
+ * the ranks' work differs by at most one matrix's.  owner_out[i] receives the
+ * rank of matrix i.  Errors: MUON_ERR_INVALID_ARG (world < 1, n_mats < 0, NULL
+ * arrays), MUON_ERR_UNSUPPORTED_SHAPE.
+ */
+MUON_API muon_status muon_partition(const muon_shape shapes[], int n_mats, int world, int owner_out[]);
+
 /* Free the workspace and the context.  Synchronises the device first. */
 MUON_API muon_status muon_destroy(void);
 

@@ -111,13 +111,15 @@ def lib():
                                         ctypes.POINTER(vp), ctypes.POINTER(muon_shape), ctypes.c_int,
                                         ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_float, ctypes.c_float, vp]
+        L.muon_partition.argtypes = [ctypes.POINTER(muon_shape), ctypes.c_int, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_int)]
         L.muon_adamw_step.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                       ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_longlong), ctypes.c_int,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_float, ctypes.c_int, vp]
         for name in ("muon_init", "muon_step", "muon_destroy", "muon_get_status", "muon_get_step_info",
                      "muon_kernel_times", "muon_debug_copy_ns_output", "muon_debug_copy_norms",
-                     "muon_plan_query", "muon_momentum_norm_noalloc", "muon_adamw_step", "muon_step_normuon"):
+                     "muon_plan_query", "muon_momentum_norm_noalloc", "muon_adamw_step", "muon_step_normuon", "muon_partition"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -232,6 +234,16 @@ def muon_plan_query(shapes, ns_steps: int = 5, check: bool = True):
     return st
 
 
+def muon_partition(shapes, world: int) -> list:
+    """Owner rank of every matrix for a sharded step over `world` ranks (host only)."""
+    shapes = [(int(r), int(c)) for r, c in shapes]
+    n = len(shapes)
+    arr = (muon_shape * max(n, 1))(*[muon_shape(r, c) for r, c in shapes])
+    out = (ctypes.c_int * max(n, 1))()
+    _check(lib().muon_partition(arr, n, int(world), out), "muon_partition")
+    return [out[i] for i in range(n)]
+
+
 def muon_kernel_times() -> dict:
     """{kind: (milliseconds, launches)} since the previous call (needs MUON_DEBUG_TIME_KERNELS)."""
     n = len(KERNEL_KINDS)
@@ -313,3 +325,6 @@ def declared_symbols() -> list:
     import re
     text = open(HEADER_PATH).read()
     return sorted(set(re.findall(r"^\s*(?:MUON_API\s+)?(?:const\s+char\*|muon_status)\s+(muon_\w+)\s*\(", text, re.M)))
+
+
+from . import zero2  # noqa: E402  (the sharded step driver uses the functions above)

@@ -4,6 +4,7 @@
 // and the launch sequence
 //   momentum_norm  ->  K x { Gram -> polynomial -> axpy (the last one fused with
 //   the weight update) }     (or the standalone update when K = 0).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -957,6 +958,29 @@ muon_status muon_step_normuon(float* const params[], const float* const grads[],
     }
     const NormuonCall nm{second_moments, beta2, eps2};
     return step_impl(params, grads, momentum_bufs, shapes, n_mats, lr, beta, nesterov, ns_steps, stream, &nm);
+}
+
+muon_status muon_partition(const muon_shape shapes[], int n_mats, int world, int owner_out[]) {
+    if (world < 1 || n_mats < 0 || (n_mats > 0 && (!shapes || !owner_out))) return MUON_ERR_INVALID_ARG;
+    if (check_shapes(shapes, n_mats) != MUON_OK) return MUON_ERR_UNSUPPORTED_SHAPE;
+    std::vector<double> cost(n_mats);
+    std::vector<int> idx(n_mats);
+    for (int i = 0; i < n_mats; ++i) {
+        const double m = std::min(shapes[i].rows, shapes[i].cols), n = std::max(shapes[i].rows, shapes[i].cols);
+        cost[i] = 3.0 * m * m * n + m * m * m;
+        idx[i] = i;
+    }
+    // largest first; equal costs keep their index order
+    std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+    std::vector<double> load(world, 0.0);
+    for (int i : idx) {
+        int best = 0;
+        for (int r = 1; r < world; ++r)
+            if (load[r] < load[best]) best = r;
+        owner_out[i] = best;
+        load[best] += cost[i];
+    }
+    return MUON_OK;
 }
 
 muon_status muon_plan_query(const muon_shape shapes[], int n_mats, int ns_steps, muon_plan_info* out) {
