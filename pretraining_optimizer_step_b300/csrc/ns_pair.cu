@@ -5,7 +5,7 @@
 // three launches of this kernel over every matrix of the step (grouped by
 // oriented shape class); the modes and their epilogues are those of
 // ns_gemm.cu:
-//   MODE_GRAM        A = s^2 X X^T               tiles on/above the diagonal, mirrored on store
+//   MODE_GRAM        A = s^2 X X^T               tiles on/above the diagonal, upper blocks stored
 //   MODE_POLY        B' = b A + c A A + a I      A symmetric: A A = A A^T, same operand both sides
 //   MODE_AXPY        X' = s B' X                 X read MN-major as the B operand
 //   MODE_AXPY_FINAL  O = s B' X in fp32, p -= lr sqrt(max(1, r/c)) O
@@ -22,6 +22,15 @@
 //   Gram/poly: tile = row blocks (2 rp, 2 rp + 1) x column blocks (2 q, 2 q + 1),
 //              rp <= q; N = 128 when column block 2 q + 1 does not exist.  The
 //              lower block of a diagonal tile is computed but not stored.
+// Symmetric storage: A and B' are stored as their 128 x 128 blocks on and above
+// the diagonal (diagonal blocks in full); nothing below is written.  A GEMM that
+// reads A or B' as an operand takes a K panel that lies below the diagonal from
+// the stored block across it, transposed: the same 64 x 128 TMA box with the
+// coordinates swapped, consumed as an MN-major operand.  The two CTAs of a pair
+// share one instruction descriptor, so a stage is read transposed on both
+// halves when its K block is at or left of the pair's first row block (the
+// diagonal block there is symmetric and stored whole, so either orientation of
+// it is correct).
 //   axpy:      tile = row blocks (2 rp, 2 rp + 1) x columns [256 ct, 256 ct + N).
 //
 // CTA layout (192 threads, persistent over the pair tiles):
@@ -94,7 +103,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Byte offsets inside the swizzled 32 x 32 subtiles the epilogue TMA maps use.
 // bf16, 64-byte rows, 64B swizzle: 16-byte unit u of row r lives at unit u ^ ((r >> 1) & 3).
 __device__ __forceinline__ uint32_t sw64_unit(int r, int u) { return r * 64 + ((u ^ ((r >> 1) & 3)) << 4); }
-__device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_unit(r, c >> 3) + ((c & 7) << 1); }
 // fp32, 128-byte rows, 128B swizzle: 16-byte unit u of row r lives at unit u ^ (r & 7).
 __device__ __forceinline__ uint32_t sw128_unit(int r, int u) { return r * 128 + ((u ^ (r & 7)) << 4); }
 __device__ __forceinline__ uint32_t sw128_elem(int r, int c) { return sw128_unit(r, c >> 2) + ((c & 3) << 2); }
@@ -181,6 +189,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const CUtensorMap* mB = &P.tmB[pt.ci];
             const int half = pt.ncols >> 1;             // this CTA's B-side rows/columns: 64 or 128
             const int b0 = pt.c0 + rank * half;         // first of them
+            // symmetric operands read from upper-block storage: first row / column block of the pair
+            const bool a_symm = P.mode != MODE_GRAM;    // poly: A; axpy: B'
+            const int a_first = pt.rb - rank;           // the pair's first row block
+            const int b_first = pt.c0 >> 7;             // the pair's first column block (poly)
             const uint32_t total_bytes = 2u * (2u * kPairPanelBytes + static_cast<uint32_t>(half) * kPairBK * 2u);
             for (int kb = 0; kb < C.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, P.timeout_ns)) {
@@ -194,18 +206,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const int k0 = kb * kPairBK;
                 const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
                 if (leader) mbar_arrive_expect_tx(&full_bar[stage], total_bytes);
+                const bool a_tr = a_symm && kb <= a_first;   // this K block is below the stored triangle
                 for (int h = 0; h < 2; ++h) {
                     if (P.inject_lost_load && leader && !injected && cluster == 0) {
                         injected = true;  // test hook: this A panel never arrives
+                    } else if (a_tr) {
+                        // MN-major: 64 of this CTA's rows (as columns of the stored block) x 128 K rows
+                        tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, pt.rb * 128 + 64 * h, k0, pt.mat);
                     } else {
                         tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, k0 + 64 * h, pt.rb * 128, pt.mat);
                     }
                 }
                 if (sym) {
-                    // K-major B half: 128 rows (box of tmA) or 64 rows (box of tmB) per K panel
-                    const CUtensorMap* mBs = half == 128 ? mA : mB;
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_3d_pair(sb + h * kPairPanelBytes, mBs, bar, k0 + 64 * h, b0, pt.mat);
+                    const bool b_tr = P.mode == MODE_POLY && kb <= b_first;
+                    if (b_tr) {
+                        // MN-major B half: one 64 x 128 panel per 64 of this CTA's N rows
+                        for (int j = 0; j < half / 64; ++j)
+                            tma_load_3d_pair(sb + j * kPairPanelBytes, mA, bar, b0 + 64 * j, k0, pt.mat);
+                    } else {
+                        // K-major B half: 128 rows (box of tmA) or 64 rows (box of tmB) per K panel
+                        const CUtensorMap* mBs = half == 128 ? mA : mB;
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d_pair(sb + h * kPairPanelBytes, mBs, bar, k0 + 64 * h, b0, pt.mat);
+                    }
                 } else {
                     // MN-major X: one 64-column x 128-K panel per 64 columns of the B half
                     for (int j = 0; j < half / 64; ++j)
@@ -228,7 +251,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         for (int t = cluster; t < P.total_tiles && !aborted; t += nclusters) {
             const PairTile pt = decode_pair_tile(P, t, 0, sym);
             const PairClass& C = P.cls[pt.ci];
-            const uint32_t idesc = idesc_bf16_f32(256, pt.ncols, sym ? 0 : 1);
+            const bool a_symm = P.mode != MODE_GRAM;
+            const int a_first = pt.rb;            // rank 0's row block = the pair's first
+            const int b_first = pt.c0 >> 7;
             if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_flag, P.timeout_ns)) {
                 latch_status(P.status, STATUS_TIMEOUT);
                 abort_flag = 1;
@@ -246,12 +271,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const uint32_t sa = tiles_base + stage * kPairStageBytes;
                 const uint32_t sb = sa + 2 * kPairPanelBytes;
+                const int a_mn = (a_symm && kb <= a_first) ? 1 : 0;
+                const int b_mn = sym ? ((P.mode == MODE_POLY && kb <= b_first) ? 1 : 0) : 1;
+                const uint32_t idesc = idesc_bf16_f32_ab(256, pt.ncols, a_mn, b_mn);
 #pragma unroll
                 for (int kk = 0; kk < kPairBK / 16; ++kk) {
-                    const uint32_t kpan = (kk >> 2) * kPairPanelBytes + (kk & 3) * 32;  // K-major: panel, 32 B per K 16
-                    const uint64_t adesc = smem_desc_sw128(sa + kpan, 16, 1024);
-                    const uint64_t bdesc = sym ? smem_desc_sw128(sb + kpan, 16, 1024)
-                                               : smem_desc_sw128(sb + kk * 2048, kPairPanelBytes, 1024);
+                    // K-major: K panel kk / 4, 32 B per 16 of K; MN-major: 64-wide atoms 16 KiB apart,
+                    // 2 KiB per 16 of K
+                    const uint32_t kpan = (kk >> 2) * kPairPanelBytes + (kk & 3) * 32;
+                    const uint64_t adesc = a_mn ? smem_desc_sw128(sa + kk * 2048, kPairPanelBytes, 1024)
+                                                : smem_desc_sw128(sa + kpan, 16, 1024);
+                    const uint64_t bdesc = b_mn ? smem_desc_sw128(sb + kk * 2048, kPairPanelBytes, 1024)
+                                                : smem_desc_sw128(sb + kpan, 16, 1024);
                     tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
                 tc_commit_pair_multicast(&empty_bar[stage], 0x3);
@@ -279,15 +310,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // loads run n_in - 1 chunks ahead; output slots alternate per committed store group):
         //   final (24 KiB): 4 input slots of fp32 32x32 weights (4 KiB) + 1 output slot (fp32 O,
         //                   for the debug copy)
-        //   gram  (8 KiB):  2 output slots of {bf16 direct, bf16 mirror}
-        //   poly  (8 KiB):  2 bf16 input slots (A) + 1 output slot of {direct, mirror}
-        //   axpy  (8 KiB):  4 output slots of bf16 direct
+        //   gram  (8 KiB):  4 output slots of bf16
+        //   poly  (8 KiB):  2 bf16 input slots (A) + 2 output slots of bf16
+        //   axpy  (8 KiB):  4 output slots of bf16
         //   axpy_o (8 KiB): 2 output slots of fp32 O
         const bool o_mode = P.mode == MODE_AXPY_O;
         const int n_in = final_mode ? 4 : (has_in ? 2 : 0);
         const int in_stride = final_mode ? 4096 : 2048;
-        const int n_out = (P.mode == MODE_GRAM || o_mode) ? 2 : (P.mode == MODE_AXPY ? 4 : 1);
-        const int out_stride = (P.mode == MODE_AXPY) ? 2048 : 4096;
+        const int n_out = final_mode ? 1 : (o_mode || P.mode == MODE_POLY) ? 2 : 4;
+        const int out_stride = (final_mode || o_mode) ? 4096 : 2048;
         uint8_t* out_base = wbase + n_in * in_stride;
         auto in_f32 = [&](int sl) { return wbase + sl * in_stride; };
         auto in_b16 = [&](int sl) { return wbase + sl * in_stride; };
@@ -465,14 +496,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                             *reinterpret_cast<uint4*>(out_slot + sw64_unit(lane, u)) = w;
                         }
                     }
-                    const bool mirror = sym && (cc0 >> 7) > pt.rb;
-                    if (mirror) {
-                        // transposed subtile: row j (= output row cc0 + j), column lane
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            *reinterpret_cast<__nv_bfloat16*>(out_slot + 2048 + sw64_elem(j, lane)) =
-                                __float2bfloat16_rn(v[j]);
-                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -488,7 +511,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                             else tma_store_2d(&P.o_maps[gm], out_slot, cc0, grow0);
                         } else {
                             tma_store_3d(&P.tmOut[pt.ci], out_slot, cc0, grow0, pt.mat);
-                            if (mirror) tma_store_3d(&P.tmOut[pt.ci], out_slot + 2048, grow0, cc0, pt.mat);
                         }
                         bulk_commit_group();
                         stores_issued = true;
