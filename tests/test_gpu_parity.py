@@ -207,3 +207,17 @@ def test_d26_full_stack_sampled():
     p, g, m, _ = workloads.make_stack("d26", "cuda")
     n = len(p)
     run_and_check(p, g, m, check_idx=[0, 4, 5, n - 6, n - 2, n - 1])
+
+
+def test_many_classes_and_matrices_span_several_launches():
+    # 10 distinct oriented shapes (two launch groups of at most 8 classes per GEMM mode) and
+    # 200 matrices (two momentum launches of at most 192 matrices)
+    base = [(64, 64), (64, 128), (128, 64), (96, 96), (64, 192), (192, 64), (128, 128), (32, 96), (96, 32),
+            (160, 160)]
+    shapes = [base[i % len(base)] for i in range(200)]
+    q = mu.muon_plan_query(shapes, 5)
+    assert q["n_classes"] == 10 and q["launches"] == 2 + 3 * 5 * 2
+    p, g, m, _ = workloads.make_custom(shapes, "cuda", tag="many")
+    run_and_check(p, g, m, check_idx=[0, 1, 5, 9, 10, 99, 150, 191, 192, 199], tol_o=small_side_tol)
+    info = mu.muon_get_step_info()
+    assert info["launches"] == q["launches"]
