@@ -105,3 +105,54 @@ def test_two_gloo_ranks_match_one_process_on_the_mean_gradient():
     for i in range(len(SHAPES)):
         assert np.allclose(res[0][0][i], params[i], rtol=0, atol=1e-6), i
         assert np.allclose(res[owner[i]][2][i], moms[i], rtol=0, atol=1e-9), i
+
+
+def _failing_worker(rank, world, port, case, out):
+    import datetime
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=2))
+    try:
+        params = [workloads.make_param("zero2", i, s, "cpu", 0) for i, s in enumerate(SHAPES)]
+        before = [p.clone() for p in params]
+
+        def broken_compute(*args, **kwargs):
+            raise RuntimeError("update failed on this rank")
+
+        compute = broken_compute if (case == "raises" and rank == 1) else oracle_compute
+        sharded = mu.zero2.ShardedMuon(params, compute=compute)
+        if case == "never_joins" and rank == 1:
+            time.sleep(6.0)  # holds the group open past the survivor's timeout, then leaves
+            out[rank] = ("left", None, None)
+            return
+        t0 = time.monotonic()
+        try:
+            sharded.step(_rank_grads(rank, 0), **HYPER)
+            out[rank] = ("ok", time.monotonic() - t0, None)
+        except RuntimeError as e:
+            # which matrices changed: a failure in phase 1 leaves every weight as it was
+            changed = [i for i, (a, b) in enumerate(zip(before, params)) if not torch.equal(a, b)]
+            out[rank] = (str(e)[:200], time.monotonic() - t0, (changed, sharded.owned))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case", ["never_joins", "raises"])
+def test_a_failed_rank_surfaces_as_an_error_on_the_others(case):
+    world = 2
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_failing_worker, args=(world, _free_port(), case, out), nprocs=world, join=True)
+        res = dict(out)
+    msg, elapsed, state = res[0]
+    assert msg != "ok", "the surviving rank finished a step its peer never completed"
+    assert elapsed < 5.0  # the process group's 2 s limit ends the wait, not the peer's exit
+    changed, owned = state
+    if case == "never_joins":
+        # the reduce-scatter never completed: no weight was touched
+        assert changed == []
+        assert res[1][0] == "left"
+    else:
+        # the peer failed after the reduce-scatter: only the survivor's own matrices moved
+        assert set(changed) <= set(owned)
+        assert "update failed" in res[1][0]
