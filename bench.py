@@ -292,26 +292,36 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    def timed(nsteps, fn):
+    def timed(nsteps, fn, per_step=None):
+        """Device time of nsteps calls of fn on the stream, max over ranks.  With a list as
+        per_step, an event recorded after every step adds each step's own time to it."""
         barrier()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1 if per_step is not None else 2)]
+        evs[0].record(stream)
         for k in range(nsteps):
             fn(k)
-        ev1.record(stream)
-        ev1.synchronize()
+            if per_step is not None:
+                evs[k + 1].record(stream)
+        evs[-1].record(stream)
+        evs[-1].synchronize()
         barrier()
-        return max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+        if per_step is not None:
+            per_step.extend(evs[k].elapsed_time(evs[k + 1]) for k in range(nsteps))
+        return max_over_ranks(evs[0].elapsed_time(evs[-1]), dist, dev)
 
     # ---- timed region 1: plain steps (the headline value)
     mu.muon_init()
     for k in range(args.warmup):
         step(k)
     mu.muon_get_status(stream)
+    step_ms = []
     with ClockSampler(local_rank) as clocks:
-        total_ms = timed(args.steps, step)
+        total_ms = timed(args.steps, step, step_ms)
     mu.muon_get_status(stream)
+    # the carried steps one by one (momentum carried, a new gradient set every step)
+    step_stats = {k: max_over_ranks(f(step_ms), dist, dev)
+                  for k, f in (("median", statistics.median), ("mean", statistics.mean), ("min", min),
+                               ("max", max))}
     info = mu.muon_get_step_info()
     ms_step = total_ms / args.steps
     flops_step = info["ns_alg_flops"]
@@ -490,7 +500,7 @@ def run_ours(args, rank, world, local_rank):
                                      else " (below 126 MB L2: small case)")),
                            "state_dtype": "fp32 p/g/m; bf16 Newton-Schulz operands, fp32 accumulation"},
                 "ns_tflops": ns_tflops, "frac_of_bf16_peak": ns_tflops / peak_tf_sus, "frac_of_bf16_burst_peak": ns_tflops / peak_tf,
-                "phase_ms_per_step": phase_ms, "timed_ms_with_kernel_events": timed_ms2 / args.steps,
+                "step_ms": step_stats, "phase_ms_per_step": phase_ms, "timed_ms_with_kernel_events": timed_ms2 / args.steps,
                 "roofline": roofline, "roofline_elementwise": roofline_hbm, "normuon": normuon, "adamw": adamw, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clocks.summary(), "gpu_launches": info["launches"] * args.steps,
                 "workspace_bytes": info["workspace_bytes"]}

@@ -221,3 +221,42 @@ def test_many_classes_and_matrices_span_several_launches():
     run_and_check(p, g, m, check_idx=[0, 1, 5, 9, 10, 99, 150, 191, 192, 199], tol_o=small_side_tol)
     info = mu.muon_get_step_info()
     assert info["launches"] == q["launches"]
+
+
+@pytest.mark.slow
+def test_d26_twenty_carried_steps():
+    # the benchmark's run: 20 consecutive d26 steps, momentum carried, a new
+    # gradient draw every step.  Every step checks every matrix's momentum
+    # against beta m + g (formed in float64 on the device, rounded once); the
+    # last step checks two matrices against the oracle run on the state the
+    # GPU reached (layer 13's q and layer 25's fc: a square and a 4:1 class)
+    name = "d26"
+    beta = 0.95
+    p, g, m, shapes = workloads.make_stack(name, "cuda")
+    n = len(p)
+    sampled = [13 * 6, 25 * 6 + 4]
+    assert shapes[sampled[0]] == (1664, 1664) and shapes[sampled[1]] == (6656, 1664)
+    steps = 20
+    for step in range(steps):
+        if step > 0:
+            g = [workloads.make_grad(name, i, s, "cuda", 0, step) for i, s in enumerate(shapes)]
+        last = step == steps - 1
+        if last:
+            p0, g0, m0 = (cpu_copy([ts[i] for i in sampled]) for ts in (p, g, m))
+        m_prev = [t.clone() for t in m]
+        mu.muon_step(p, g, m, lr=0.02, beta=beta, nesterov=True, ns_steps=5)
+        mu.muon_get_status()
+        bf = float(np.float32(beta))
+        for i in range(n):
+            exact = (bf * m_prev[i].double() + g[i].double())
+            err = (m[i].double() - exact).abs()
+            bound = 2.5e-7 * exact.abs() + 1.2e-7 * (bf * m_prev[i].double().abs() + g[i].double().abs())
+            assert bool((err <= bound).all()), (step, i)
+        del m_prev
+        if last:
+            for j, i in enumerate(sampled):
+                o = torch.empty_like(p[i])
+                mu.muon_debug_copy_ns_output(i, o)
+                torch.cuda.synchronize()
+                check_matrix(i, p0[j], g0[j], m0[j], p[i].cpu().numpy(), m[i].cpu().numpy(), o.cpu().numpy(),
+                             0.02, beta, True, 5, DEFAULT)
