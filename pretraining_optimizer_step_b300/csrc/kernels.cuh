@@ -72,9 +72,12 @@ constexpr int kGemmThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilo
 constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 constexpr int kMaxClasses = 8;
 
+// Symmetric results (A, B) are computed on tiles on and above the diagonal.  ns_gemm_kernel
+// mirrors them below it; ns_pair_kernel stores the upper 128 x 128 blocks only and folds a I
+// into B, so its axpy modes compute s B' X with B' = B + a I.
 enum GemmMode : int {
-    MODE_GRAM = 0,        // A = s^2 X X^T (upper tiles, mirrored)
-    MODE_POLY = 1,        // B = b A + c A A (upper tiles, mirrored)
+    MODE_GRAM = 0,        // A = s^2 X X^T
+    MODE_POLY = 1,        // B = b A + c A A
     MODE_AXPY = 2,        // X' = s (a X + B X)
     MODE_AXPY_FINAL = 3,  // O = s (a X + B X); p -= scale O
     MODE_AXPY_O = 4,      // O = s (a X + B X) written in fp32 (stored layout) for the NorMuon pass
