@@ -120,8 +120,12 @@ MUON_API muon_status muon_init(const muon_config* cfg);
  * The host arrays are read during the call only.  A matrix must not alias
  * another one of the same call.  Matrices of equal oriented shape are batched
  * into the same launches.  When the list of shapes differs from the previous
- * call's, the workspace is rebuilt, which synchronises `stream`; otherwise the
- * call never blocks the host.  Errors: MUON_ERR_NOT_INITIALIZED,
+ * call's, the workspace is rebuilt; when the weight pointers differ, their
+ * tensor maps are re-encoded; both synchronise `stream`.  Otherwise the call
+ * only enqueues kernels on `stream` and never blocks the host, so after one
+ * uncaptured call with the same shapes and weight pointers a step can be
+ * captured into a CUDA graph and replayed, with each step's gradients copied
+ * into the captured gradient buffers.  Errors: MUON_ERR_NOT_INITIALIZED,
  * MUON_ERR_INVALID_ARG, MUON_ERR_UNSUPPORTED_SHAPE, MUON_ERR_MISALIGNED,
  * MUON_ERR_OUT_OF_MEMORY, MUON_ERR_CUDA.  On an argument error nothing is
  * enqueued.

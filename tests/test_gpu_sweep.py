@@ -58,3 +58,26 @@ def test_sweep_sampled(name):
 def test_d20_sampled():
     n = len(workloads.config_shapes("d20"))
     run_case("d20", [0, 4, 5, n - 2, n - 1])
+
+
+@pytest.mark.slow
+def test_largest_sweep_shape_against_the_closed_form():
+    # the largest matrices of the configurations (the 4:1 sweep at n = 8192: 32768 x 8192, read
+    # transposed), one low-rank and one full-rank gradient; the fp64 oracle would need minutes
+    # per matrix, so O is checked against the closed form of the same iteration (its helper is
+    # pinned to the oracle on small shapes) at the same 2e-2 bound, and p' against p - lr s O_ref
+    from closed_form import closed_form_o
+    from gpu_util import TOL_P, rel_fro
+    name = "sweep_8192_tall"
+    p, g, m, shapes = workloads.make_stack(name, "cuda", indices=[0, 1])
+    assert shapes[0] == (32768, 8192)
+    p0, g0, m0 = ([t.cpu().numpy() for t in ts] for ts in (p, g, m))
+    run_gpu_step(p, g, m, keep_o=False)
+    for i in range(2):
+        o = torch.empty_like(p[i])
+        mu.muon_debug_copy_ns_output(i, o)
+        torch.cuda.synchronize()
+        O_ref = closed_form_o(g0[i], m0[i], 0.95, oracle.DEFAULT_COEFFS)
+        assert rel_fro(o.cpu().numpy(), O_ref) <= TOL_O, i
+        p_ref = p0[i].astype(np.float64) - np.float32(0.02) * 2.0 * O_ref
+        assert rel_fro(p[i].cpu().numpy(), p_ref) <= TOL_P, i

@@ -243,3 +243,17 @@ def test_pins_catch_planted_mistakes(name):
         with oracle.using_library(so_path):
             failed = _run_pins()
     assert failed, f"mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("shape", [(48, 48), (64, 200), (200, 64), (8, 96)])
+def test_closed_form_helper_matches_the_oracle(shape):
+    # the closed form the large GPU cases are checked against agrees with the
+    # step-by-step oracle (both fp64) on shapes the oracle finishes at once
+    from closed_form import closed_form_o
+    rng = np.random.default_rng(sum(shape))
+    g = (rng.standard_normal(shape) * 1e-3).astype(np.float32)
+    m = (rng.standard_normal(shape) * 1e-3).astype(np.float32)
+    p = (rng.standard_normal(shape) * 0.05).astype(np.float32)
+    _, _, O = oracle.muon_matrix(p, g, m, lr=np.float32(0.02), beta=np.float32(0.95), nesterov=True, ns_steps=5)
+    ref = closed_form_o(g, m, 0.95, oracle.DEFAULT_COEFFS)
+    assert np.linalg.norm(ref - O) <= 1e-10 * np.linalg.norm(O)
