@@ -120,7 +120,9 @@ struct GemmParams {
 // Per stored row i of O (fp32, stored r x c): v_mean = mean_j O_ij^2, V_i <- b2 V_i + (1 - b2) v_mean,
 // step_i = 1 / sqrt(V_i + eps); per matrix: ratio = sqrt(sum v_mean) / max(sqrt(sum v_mean step^2), 1e-10).
 // Then p_ij -= lr aspect step_i ratio O_ij.
-constexpr int kNormRowsPerCta = 8;           // one warp per row, 256 threads
+constexpr int kNormWarps = 8;                // 256 threads
+constexpr int kNormRowsPerWarp = 4;
+constexpr int kNormRowsPerCta = kNormWarps * kNormRowsPerWarp;
 struct NormuonMat {
     const float* O;       // stored rows x cols (workspace)
     float* V;             // caller-owned second moments, rows floats

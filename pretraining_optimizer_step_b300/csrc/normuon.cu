@@ -11,10 +11,11 @@
 //   ratio = sqrt(sum_i v_mean_i) / max(sqrt(sum_i v_mean_i step_i^2), 1e-10)
 //   p_ij <- p_ij - lr sqrt(max(1, r/c)) step_i ratio O_ij       (keeps ||O||_F)
 //
-// normuon_rows_kernel: one warp per stored row (8 rows per CTA) reads the row
+// normuon_rows_kernel: one warp per stored row (4 rows per warp, 32 per CTA) reads the row
 //   of O (fp32, 16-byte loads), reduces its squares in a fixed order, updates V
 //   and writes step_i; the last CTA of a matrix (atomic ticket) adds the CTAs'
-//   double partial sums in index order and publishes ratio.  Deterministic.
+//   double partial sums, spread over its threads in a fixed order, and
+//   publishes ratio.  Deterministic.
 // normuon_update_kernel: one CTA per 64 x 64 stored tile applies the update
 //   (and writes O' = step ratio O when the debug copy is kept).
 #include "kernels.cuh"
@@ -37,34 +38,45 @@ __device__ __forceinline__ int find_normuon_mat(const NormuonParams& P, int x, b
 }  // namespace
 
 __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant__ NormuonParams P) {
-    __shared__ double warp_old[kNormRowsPerCta], warp_new[kNormRowsPerCta];
+    __shared__ double warp_old[kNormWarps], warp_new[kNormWarps];
     __shared__ int is_last;
     const int cta = blockIdx.x;
     const NormuonMat& M = P.mats[find_normuon_mat(P, cta, true)];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = (cta - M.cta_begin) * kNormRowsPerCta + warp;
-    double s_old = 0.0, s_new = 0.0;
-    if (row < M.rows) {
+    double s_old = 0.0, s_new = 0.0;  // lane 0: this warp's rows, added in row order
+    for (int rw = 0; rw < kNormRowsPerWarp; ++rw) {
+        const int row = (cta - M.cta_begin) * kNormRowsPerCta + rw * kNormWarps + warp;
+        if (row >= M.rows) break;
         const float4* o4 = reinterpret_cast<const float4*>(M.O + static_cast<size_t>(row) * M.cols);
-        float acc = 0.f;
-        for (int q = lane; q < (M.cols >> 2); q += 32) {
-            const float4 o = __ldcg(o4 + q);
-            acc = fmaf(o.x, o.x, acc);
-            acc = fmaf(o.y, o.y, acc);
-            acc = fmaf(o.z, o.z, acc);
-            acc = fmaf(o.w, o.w, acc);
+        // four independent sums, so four loads per lane are in flight
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        const int nq = M.cols >> 2;
+        int q = lane;
+        for (; q + 96 < nq; q += 128) {
+            const float4 o0 = __ldcg(o4 + q), o1 = __ldcg(o4 + q + 32);
+            const float4 o2 = __ldcg(o4 + q + 64), o3 = __ldcg(o4 + q + 96);
+            a0 = fmaf(o0.w, o0.w, fmaf(o0.z, o0.z, fmaf(o0.y, o0.y, fmaf(o0.x, o0.x, a0))));
+            a1 = fmaf(o1.w, o1.w, fmaf(o1.z, o1.z, fmaf(o1.y, o1.y, fmaf(o1.x, o1.x, a1))));
+            a2 = fmaf(o2.w, o2.w, fmaf(o2.z, o2.z, fmaf(o2.y, o2.y, fmaf(o2.x, o2.x, a2))));
+            a3 = fmaf(o3.w, o3.w, fmaf(o3.z, o3.z, fmaf(o3.y, o3.y, fmaf(o3.x, o3.x, a3))));
         }
+        for (; q < nq; q += 32) {
+            const float4 o = __ldcg(o4 + q);
+            a0 = fmaf(o.w, o.w, fmaf(o.z, o.z, fmaf(o.y, o.y, fmaf(o.x, o.x, a0))));
+        }
+        float acc = (a0 + a1) + (a2 + a3);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        const double v_mean = static_cast<double>(acc) / M.cols;
-        const double Vn = static_cast<double>(P.beta2) * M.V[row] + (1.0 - static_cast<double>(P.beta2)) * v_mean;
-        const double step = 1.0 / sqrt(Vn + static_cast<double>(P.eps));
+        // fp64 runs at a small fraction of the fp32 rate: one lane does the row's division and root
         if (lane == 0) {
+            const double v_mean = static_cast<double>(acc) / M.cols;
+            const double Vn = static_cast<double>(P.beta2) * M.V[row] + (1.0 - static_cast<double>(P.beta2)) * v_mean;
+            const double step = 1.0 / sqrt(Vn + static_cast<double>(P.eps));
             M.V[row] = static_cast<float>(Vn);
             P.step[P.row_base[M.pos] + row] = static_cast<float>(step);
+            s_old += v_mean;
+            s_new += v_mean * step * step;
         }
-        s_old = v_mean;
-        s_new = v_mean * step * step;
     }
     if (lane == 0) {
         warp_old[warp] = s_old;
@@ -73,7 +85,7 @@ __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant
     __syncthreads();
     if (threadIdx.x == 0) {
         double a = 0.0, b = 0.0;
-        for (int w = 0; w < kNormRowsPerCta; ++w) {
+        for (int w = 0; w < kNormWarps; ++w) {
             a += warp_old[w];
             b += warp_new[w];
         }
@@ -84,15 +96,33 @@ __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant
         is_last = ticket == static_cast<unsigned int>(M.nctas - 1) ? 1 : 0;
     }
     __syncthreads();
-    if (!is_last || threadIdx.x != 0) return;
+    if (!is_last) return;
+    // Last CTA of the matrix: every thread adds a fixed strided subset of the CTAs' partials,
+    // then a fixed xor tree per warp and the warp sums in index order (deterministic)
     __threadfence();
     double a = 0.0, b = 0.0;
-    for (int k = 0; k < M.nctas; ++k) {
+    for (int k = threadIdx.x; k < M.nctas; k += blockDim.x) {
         a += __ldcg(P.partials + 2 * (M.cta_begin + k));
         b += __ldcg(P.partials + 2 * (M.cta_begin + k) + 1);
     }
-    const double nb = sqrt(b);
-    P.ratio[M.pos] = static_cast<float>(sqrt(a) / (nb > 1e-10 ? nb : 1e-10));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, off);
+        b += __shfl_xor_sync(0xffffffffu, b, off);
+    }
+    if (lane == 0) {
+        warp_old[warp] = a;  // thread 0 finished reading these before the barrier above
+        warp_new[warp] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    double sa = 0.0, sb = 0.0;
+    for (int w = 0; w < kNormWarps; ++w) {
+        sa += warp_old[w];
+        sb += warp_new[w];
+    }
+    const double nb = sqrt(sb);
+    P.ratio[M.pos] = static_cast<float>(sqrt(sa) / (nb > 1e-10 ? nb : 1e-10));
     P.counters[M.pos] = 0u;
 }
 

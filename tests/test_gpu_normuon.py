@@ -110,3 +110,29 @@ def test_argument_errors():
     torch.cuda.synchronize()
     for a, b in zip(before, p + m + V):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("case", ["d2", "ragged"])
+def test_row_statistics_are_consistent_with_the_update(case):
+    # With a zero state, V'_i = (1 - beta2) mean_j O_ij^2, and the debug copy is O' = step_i ratio O
+    # with step_i = 1 / sqrt(V'_i + eps2).  So every stored row gives the same value
+    #   mean_j O'_ij^2 (V'_i + eps2) (1 - beta2) / V'_i  =  ratio^2,
+    # to float32 rounding.  A row sum that missed or double-counted part of its row (a tile, a
+    # ragged edge, a 32-row group of a transposed matrix) breaks the equality for that row.
+    if case == "d2":
+        p, g, m, shapes = workloads.make_stack("d2", "cuda")
+    else:
+        shapes = [(136, 200), (200, 136), (264, 264), (392, 1032), (1032, 392), (8, 1024), (1024, 8)]
+        p, g, m, _ = workloads.make_custom(shapes, "cuda", tag="nmrows")
+    V = zeros_state(shapes)
+    mu.muon_step_normuon(p, g, m, V, lr=0.02, beta=0.95, nesterov=True, ns_steps=5, beta2=BETA2, eps2=EPS2)
+    mu.muon_get_status()
+    for i, (r, c) in enumerate(shapes):
+        Op = torch.empty_like(p[i])
+        mu.muon_debug_copy_ns_output(i, Op)
+        torch.cuda.synchronize()
+        Op = Op.double().cpu().numpy()
+        Vi = V[i].double().cpu().numpy()
+        assert np.all(Vi > 0), i
+        r2 = np.mean(Op * Op, axis=1) * (Vi + EPS2) * (1.0 - float(np.float32(BETA2))) / Vi
+        assert np.max(np.abs(r2 / np.median(r2) - 1.0)) <= 1e-4, (i, float(np.max(np.abs(r2 / np.median(r2) - 1.0))))
