@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant
     const int cta = blockIdx.x;
     const NormuonMat& M = P.mats[find_normuon_mat(P, cta, true)];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    double s_old = 0.0, s_new = 0.0;  // lane 0: this warp's rows, added in row order
+    float s_old = 0.f, s_new = 0.f;  // lane 0: this warp's rows, added in row order
     for (int rw = 0; rw < kNormRowsPerWarp; ++rw) {
         const int row = (cta - M.cta_begin) * kNormRowsPerCta + rw * kNormWarps + warp;
         if (row >= M.rows) break;
@@ -67,20 +67,21 @@ __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant
         float acc = (a0 + a1) + (a2 + a3);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        // fp64 runs at a small fraction of the fp32 rate: one lane does the row's division and root
+        // fp32 (IEEE division and square root): the fp64 pipe of this part costs a full warp
+        // instruction slot per operation even for one lane, and the row path would be bound by it
         if (lane == 0) {
-            const double v_mean = static_cast<double>(acc) / M.cols;
-            const double Vn = static_cast<double>(P.beta2) * M.V[row] + (1.0 - static_cast<double>(P.beta2)) * v_mean;
-            const double step = 1.0 / sqrt(Vn + static_cast<double>(P.eps));
-            M.V[row] = static_cast<float>(Vn);
-            P.step[P.row_base[M.pos] + row] = static_cast<float>(step);
+            const float v_mean = acc / static_cast<float>(M.cols);
+            const float Vn = fmaf(P.beta2, M.V[row], (1.0f - P.beta2) * v_mean);
+            const float step = 1.0f / sqrtf(Vn + P.eps);
+            M.V[row] = Vn;
+            P.step[P.row_base[M.pos] + row] = step;
             s_old += v_mean;
             s_new += v_mean * step * step;
         }
     }
     if (lane == 0) {
-        warp_old[warp] = s_old;
-        warp_new[warp] = s_new;
+        warp_old[warp] = static_cast<double>(s_old);
+        warp_new[warp] = static_cast<double>(s_new);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
