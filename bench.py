@@ -508,6 +508,70 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+def run_sweep(args) -> int:
+    """Newton-Schulz throughput across the shape sweep (n x n, 4n x n, n x 4n for n = 256 ... 8192),
+    one GPU.  Each shape runs with an even number of matrices (low-rank and full-rank gradients
+    alternate) bounded so that the fp32 state and the bf16 workspace stay under about 40 GB; every
+    step is timed alone with CUDA events, with a 256 MB write between steps (outside the events) so
+    that no step starts with its operands in L2.  Prints one JSON object with a row per shape."""
+    import torch
+    import pretraining_optimizer_step_b300 as mu
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_bw = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    rows = []
+    for name in workloads.sweep_names():
+        all_shapes = workloads.config_shapes(name)
+        r, c = all_shapes[0]
+        mm, nn = min(r, c), max(r, c)
+        per_matrix = 12 * r * c + 4 * mm * nn + 4 * mm * mm
+        count = max(2, min(len(all_shapes), int(40e9 // per_matrix)))
+        count -= count % 2
+        p, g, m, shapes = workloads.make_stack(name, dev, indices=list(range(count)))
+        mu.muon_init(debug_flags=mu.MUON_DEBUG_TIME_KERNELS)
+        stream = torch.cuda.Stream(device=dev)
+        sargs = mu.StepArgs(p, g, m, shapes)
+        for _ in range(args.warmup):
+            mu.muon_step(sargs, stream=stream)
+        mu.muon_get_status(stream)
+        mu.muon_kernel_times()
+        times = []
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            mu.muon_step(sargs, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        mu.muon_get_status(stream)
+        kt = mu.muon_kernel_times()
+        info = mu.muon_get_step_info()
+        q = mu.muon_plan_query(shapes, workloads.HYPER["ns_steps"])
+        ns_ms = sum(kt[k][0] for k in ("gram", "poly", "axpy", "axpy_update")) / args.steps
+        mom_ms = kt["momentum_norm"][0] / args.steps
+        ms = statistics.median(times)
+        rows.append({"workload": name, "shape": [r, c], "matrices": count, "ms_per_step": ms,
+                     "ns_tflops": info["ns_alg_flops"] / (ns_ms * 1e-3) / 1e12,
+                     "ns_frac_of_sustained_bf16": info["ns_alg_flops"] / (ns_ms * 1e-3) / 1e12 / peak_sus,
+                     "executed_over_alg_flops": q["ns_executed_flops"] / q["ns_alg_flops"],
+                     "momentum_gbs": 14.0 * count * r * c / (mom_ms * 1e-3) / 1e9,
+                     "momentum_frac_of_hbm": 14.0 * count * r * c / (mom_ms * 1e-3) / 1e9 / peak_bw,
+                     "launches_per_step": info["launches"]})
+        mu.muon_destroy()
+        del p, g, m, sargs
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": rows, "peak_source": peak_src, "steps": args.steps, "warmup": args.warmup,
+                      "timing": "median of per-step CUDA-event times; 256 MB written between steps"}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,7 +582,11 @@ def main():
                     help="d26 (the measured workload) or a smaller case for profiling: d2, d12, d20, sweep_*")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one GPU: Newton-Schulz throughput over the square / 4:1 shape sweep (not the benchmark line)")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
