@@ -33,6 +33,10 @@
  *    an out-of-range tile) are latched in a device status word and returned by
  *    muon_get_status.
  *  - One process-global context; the functions are not thread-safe.
+ *  - The steps of a context share one workspace (and the NorMuon buffers), and
+ *    a call orders its work only after earlier work on its own `stream`.  Steps
+ *    issued on different streams must therefore be ordered by the caller (an
+ *    event, or one stream for all of them); steps that overlap on the GPU race.
  */
 #ifndef MUON_H
 #define MUON_H
