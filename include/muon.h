@@ -125,7 +125,8 @@ MUON_API muon_status muon_init(const muon_config* cfg);
  * another one of the same call.  Matrices of equal oriented shape are batched
  * into the same launches.  When the list of shapes differs from the previous
  * call's, the workspace is rebuilt; when the weight pointers differ, their
- * tensor maps are re-encoded; both synchronise `stream`.  Otherwise the call
+ * tensor maps are re-encoded.  Both synchronise the device (a step still
+ * running on another stream may use the old ones).  Otherwise the call
  * only enqueues kernels on `stream` and never blocks the host, so after one
  * uncaptured call with the same shapes and weight pointers a step can be
  * captured into a CUDA graph and replayed, with each step's gradients copied

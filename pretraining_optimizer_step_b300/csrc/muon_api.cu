@@ -635,7 +635,8 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
 
     if (!same_shapes(ctx->plan, shapes, n_mats)) {
         if (ctx->plan) {
-            if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+            // work of earlier steps, on any stream, may still use the old workspace
+            if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
             free_plan(ctx->plan);
             ctx->plan = nullptr;
         }
@@ -722,8 +723,8 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                 if (encode_f32_map(ctx->encode, &pm[k], params[i], shapes[i].rows, shapes[i].cols) != MUON_OK)
                     return MUON_ERR_CUDA;
             }
-            // launches already enqueued may still read the previous maps
-            if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+            // launches already enqueued, on any stream, may still read the previous maps
+            if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
             if (cudaMemcpy(P->p_maps, pm.data(), n_mats * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
                 return MUON_ERR_CUDA;
             P->mapped_p.assign(params, params + n_mats);
