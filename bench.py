@@ -62,7 +62,7 @@ def load_peaks():
 class ClockSampler:
     """Samples SM clocks, power and clock-event reasons during a timed region.
 
-    Uses `nvidia-smi --query-gpu=... -lms 200` in a child process (the sampler
+    Uses `nvidia-smi --query-gpu=... -lms 50` in a child process (the sampler
     is started before the region and stopped after it); if nvidia-smi is not on
     PATH, NVML through pynvml every 100 ms instead."""
 
@@ -89,14 +89,14 @@ class ClockSampler:
             return False
         self._proc = subprocess.Popen(
             [exe, "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-             "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+             "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         # wait (up to 5 s) for the sampler's first line, so that it is live when
         # the timed region starts; that line was taken before the region and is dropped
         import select
         ready, _, _ = select.select([self._proc.stdout], [], [], 5.0)
         if ready:
             self._proc.stdout.readline()
-        self.source = "nvidia-smi -lms 200"
+        self.source = "nvidia-smi -lms 50"
         return True
 
     def _parse_smi(self, text):
