@@ -40,3 +40,23 @@ def test_reference_arm_on_a_non_zero_rank_is_silent():
                     "--workload", "d2")
     assert out.returncode == 0, out.stderr[-2000:]
     assert out.stdout.strip() == ""
+
+
+def test_clock_sampler_parses_smi_lines():
+    # the sampler's parser on lines in nvidia-smi's csv,noheader,nounits format: median SM clock,
+    # max clock, max power, and every throttle reason that was active in any sample
+    sys.path.insert(0, ROOT)
+    import bench
+    s = bench.ClockSampler(0)
+    s.source = "test"
+    s._parse_smi("\n".join([
+        "0, 1395, 2032, 612.40, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1410, 2032, 598.10, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1650, 2032, 420.00, 0x0000000000000000, Not Active, Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2032, 400.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]))
+    out = s.summary()
+    assert out["samples"] == 3 and out["sm_mhz"] == 1410.0 and out["sm_max_mhz"] == 2032.0
+    assert out["power_w_max"] == 612.40
+    assert out["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
