@@ -136,3 +136,14 @@ def test_row_statistics_are_consistent_with_the_update(case):
         assert np.all(Vi > 0), i
         r2 = np.mean(Op * Op, axis=1) * (Vi + EPS2) * (1.0 - float(np.float32(BETA2))) / Vi
         assert np.max(np.abs(r2 / np.median(r2) - 1.0)) <= 1e-4, (i, float(np.max(np.abs(r2 / np.median(r2) - 1.0))))
+
+
+@pytest.mark.parametrize("ns_steps,tol", [(1, 5e-3), (2, TOL_O)])
+def test_short_iterations_on_ragged_shapes(ns_steps, tol):
+    # with one iteration the launch that writes O is also the first one, so it applies the
+    # 1/||u|| scale itself; the single iteration is checked tightly (bf16 rounding of X0 gives
+    # about 1.7e-3), as for muon_step
+    shapes = [(136, 200), (200, 136), (264, 264), (8, 1024), (1024, 8)]
+    p, g, m, _ = workloads.make_custom(shapes, "cuda", tag="nmshort")
+    V = [torch.rand(r, device="cuda") * 1e-3 for r, _ in shapes]
+    step_and_check(p, g, m, V, ns_steps=ns_steps, tol_o=tol)

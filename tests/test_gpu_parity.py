@@ -260,3 +260,17 @@ def test_d26_twenty_carried_steps():
                 torch.cuda.synchronize()
                 check_matrix(i, p0[j], g0[j], m0[j], p[i].cpu().numpy(), m[i].cpu().numpy(), o.cpu().numpy(),
                              0.02, beta, True, 5, DEFAULT)
+
+
+def test_sixteen_row_table_runs_sixteen_iterations():
+    # the longest table the context takes: 16 rows alternating the default quintic with the
+    # cubic Newton-Schulz step (a convergent mix), so every one of the 48 GEMM launches must pick
+    # up its own row and the ping-pong buffers alternate through an even count
+    cubic = (1.5, -0.5, 0.0)
+    rows = [oracle.DEFAULT_ROW if k % 2 == 0 else cubic for k in range(16)]
+    mu.muon_destroy()
+    mu.muon_init(coeffs=rows, debug_flags=mu.MUON_DEBUG_KEEP_O, wait_timeout_s=2.0)
+    p, g, m, shapes = workloads.make_stack("d2", "cuda")
+    assert mu.muon_plan_query(shapes, 16)["launches"] == 1 + 3 * 16
+    run_and_check(p, g, m, coeffs=np.array(rows), ns_steps=16)
+    assert mu.muon_get_step_info()["launches"] == 1 + 3 * 16
