@@ -2,6 +2,7 @@
 declares, validates arguments, and its host-only planner counts work the way
 the tiling defines it (checked against an independent enumeration here)."""
 import ctypes
+import os
 import math
 
 import pytest
@@ -209,3 +210,45 @@ def test_adamw_set_shapes():
     shapes = workloads.adamw_shapes("d26")
     assert shapes[0] == (32768, 1664) and shapes[1] == (32768, 1664)
     assert sum(math.prod(s) for s in shapes) == 2 * 32768 * 1664 + 52 + 24 + 1
+
+
+def test_header_constants_match_the_binding():
+    # every MUON_* value the header defines has the same value in the Python binding
+    import re
+    text = open(mu.HEADER_PATH).read()
+    pairs = re.findall(r"\b(MUON_[A-Z0-9_]+)\s*=\s*(\d+)", text)
+    assert len(pairs) >= 18
+    for name, value in pairs:
+        assert getattr(mu, name) == int(value), name
+
+
+def test_struct_layouts_match_the_header():
+    # the ctypes structures have the sizes and field offsets a C compiler gives the header's
+    import shutil
+    import subprocess
+    import tempfile
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    structs = {"muon_shape": mu.muon_shape, "muon_config": mu.muon_config, "muon_step_info": mu.muon_step_info,
+               "muon_plan_info": mu.muon_plan_info}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "muon.h"', "int main(void) {"]
+    for sname, cls in structs.items():
+        lines.append(f'printf("{sname} sizeof %zu\\n", sizeof({sname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{sname} {fname} %zu\\n", offsetof({sname}, {fname}));')
+    lines += ["return 0;", "}"]
+    build = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "_build", "tests")
+    os.makedirs(build, exist_ok=True)
+    with tempfile.TemporaryDirectory(dir=build) as tmp:
+        src, exe = os.path.join(tmp, "layout.c"), os.path.join(tmp, "layout")
+        open(src, "w").write("\n".join(lines) + "\n")
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(mu.HEADER_PATH), "-o", exe, src], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    seen = 0
+    for ln in out.splitlines():
+        sname, field, value = ln.split()
+        cls = structs[sname]
+        got = ctypes.sizeof(cls) if field == "sizeof" else getattr(cls, field).offset
+        assert got == int(value), (sname, field, got, value)
+        seen += 1
+    assert seen == sum(len(c._fields_) + 1 for c in structs.values())

@@ -105,6 +105,12 @@ MUTANTS = {
 }
 
 
+def _scratch_dir():
+    """Build folder for throwaway mutant libraries, inside the repository (git-ignored)."""
+    d = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "_build", "tests")
+    os.makedirs(d, exist_ok=True)
+    return d
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_normuon_pins_catch_planted_mistakes(name):
     if shutil.which("gcc") is None:
@@ -112,7 +118,7 @@ def test_normuon_pins_catch_planted_mistakes(name):
     old, new = MUTANTS[name]
     src = open(oracle.source_path()).read()
     assert src.count(old) == 1, f"mutation anchor not unique/present: {old!r}"
-    with tempfile.TemporaryDirectory() as tmp:
+    with tempfile.TemporaryDirectory(dir=_scratch_dir()) as tmp:
         c_path = os.path.join(tmp, "mutant.c")
         so_path = os.path.join(tmp, "libmutant.so")
         open(c_path, "w").write(src.replace(old, new))
