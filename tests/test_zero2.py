@@ -84,7 +84,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_match_one_process_on_the_mean_gradient():
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
@@ -140,7 +140,7 @@ def _failing_worker(rank, world, port, case, out):
 @pytest.mark.parametrize("case", ["never_joins", "raises"])
 def test_a_failed_rank_surfaces_as_an_error_on_the_others(case):
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_failing_worker, args=(world, _free_port(), case, out), nprocs=world, join=True)
         res = dict(out)
