@@ -228,14 +228,15 @@ def test_d26_twenty_carried_steps():
     # the benchmark's run: 20 consecutive d26 steps, momentum carried, a new
     # gradient draw every step.  Every step checks every matrix's momentum
     # against beta m + g (formed in float64 on the device, rounded once); the
-    # last step checks two matrices against the oracle run on the state the
-    # GPU reached (layer 13's q and layer 25's fc: a square and a 4:1 class)
+    # last step checks all six matrices of layers 0, 13 and 25 (q, k, v, o, the
+    # 4:1 MLP input and the 1:4 MLP output) against the oracle run on the state
+    # the GPU reached after 19 carried steps
     name = "d26"
     beta = 0.95
     p, g, m, shapes = workloads.make_stack(name, "cuda")
     n = len(p)
-    sampled = [13 * 6, 25 * 6 + 4]
-    assert shapes[sampled[0]] == (1664, 1664) and shapes[sampled[1]] == (6656, 1664)
+    sampled = [6 * layer + k for layer in (0, 13, 25) for k in range(6)]
+    assert shapes[sampled[4]] == (6656, 1664) and shapes[sampled[5]] == (1664, 6656)
     steps = 20
     for step in range(steps):
         if step > 0:
