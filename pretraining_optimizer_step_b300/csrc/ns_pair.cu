@@ -361,9 +361,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 }
                 in_pending_bits |= 1u << slot;
             };
-            if (has_in && lane == 0)
+            if (has_in && lane == 0) {
+                // the final launch stores the updated weights from these slots: the previous
+                // tile's stores must have read them before the new loads land
+                if (final_mode) bulk_wait_group_read0();
                 for (int ch = 0; ch < n_in && ch < nch; ++ch)
                     if (live(ch)) issue_in(ch);
+            }
             const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], acc_phase, &abort_flag,
                                                                          P.timeout_ns));
             if (!ready) {
