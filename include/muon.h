@@ -86,11 +86,9 @@ enum {
     MUON_DEBUG_KEEP_O = 1,            /* also write O (fp32, stored layout) for muon_debug_copy_ns_output */
     MUON_DEBUG_POISON_WORKSPACE = 2,  /* fill the bf16 workspace with NaN before every step */
     MUON_DEBUG_TIME_KERNELS = 4,      /* record CUDA events around every launch (muon_kernel_times) */
-    MUON_DEBUG_INJECT_LOST_LOAD = 8,  /* test hook: one operand load of the first Gram launch is never
+    MUON_DEBUG_INJECT_LOST_LOAD = 8   /* test hook: one operand load of the first Gram launch is never
                                          issued, so the consumer's bounded wait must expire and the step
                                          reports MUON_ERR_DEVICE_TIMEOUT; the result is then invalid */
-    MUON_DEBUG_SINGLE_CTA_GEMM = 16   /* ablation: run the Newton-Schulz GEMMs as 128 x 256 single-CTA
-                                         tiles instead of 256 x 256 CTA-pair tiles (same results) */
 };
 
 typedef struct muon_config {
@@ -158,8 +156,7 @@ MUON_API muon_status muon_step(float* const params[], const float* const grads[]
  *   beta2 in [0, 1), eps2 >= 0; ns_steps >= 1; other arguments as muon_step.
  * O is materialised in an fp32 workspace (one more allocation of the size of
  * the weights, made by the first call on a shape list); the per-row reduction
- * is deterministic.  Not available with MUON_DEBUG_SINGLE_CTA_GEMM
- * (MUON_ERR_INVALID_ARG).  With MUON_DEBUG_KEEP_O, muon_debug_copy_ns_output
+ * is deterministic.  With MUON_DEBUG_KEEP_O, muon_debug_copy_ns_output
  * returns the scaled update step_i ratio O.  Errors as muon_step.
  */
 MUON_API muon_status muon_step_normuon(float* const params[], const float* const grads[],
@@ -214,9 +211,9 @@ MUON_API muon_status muon_get_step_info(muon_step_info* out);
  * oriented shape classes (matrices with equal (min side, max side,
  * transposed) share launches), kernel launches per step, workspace bytes,
  * algorithmic Newton-Schulz flops (3 m^2 n + m^3 per matrix and iteration),
- * executed tensor-core flops of the 128 x 256 tiles (diagonal and ragged tiles
- * included), algorithmic elementwise bytes (22 per element), momentum CTAs, and
- * tiles per Gram/polynomial launch and per axpy launch.
+ * executed tensor-core flops of the 256-row CTA-pair tiles (diagonal and ragged
+ * tiles included), algorithmic elementwise bytes (22 per element), momentum
+ * CTAs, and pair tiles per Gram/polynomial launch and per axpy launch.
  * ns_steps is checked against the current context's table (16 rows without one).
  */
 typedef struct muon_plan_info {
@@ -291,8 +288,8 @@ MUON_API muon_status muon_adamw_step(float* const params[], const float* const g
  * and stall other streams) once it is serving, and code running where
  * allocation is forbidden.  It runs the first stage of muon_step on the
  * caller's buffers.  It allocates nothing, needs no muon_init, and keeps its
- * scratch (per-tile norm partials, per-matrix tickets and constants) in one
- * fixed array inside the library:
+ * scratch (per-tile norm partials, per-matrix tickets and 1/(||u|| + eps)) in
+ * one fixed array inside the library:
  *
  *   m' = beta m + g (stored back into momentum_bufs[i]); EMA form with
  *        momentum_mode MUON_MOMENTUM_EMA, as in muon_step
@@ -313,12 +310,15 @@ MUON_API muon_status muon_adamw_step(float* const params[], const float* const g
  * Limits (MUON_ERR_SCRATCH_LIMIT beyond them, checked before anything is
  * enqueued): n_mats <= 1024, and every group of 192 consecutive matrices
  * covers at most 262144 tiles of 64 x 64 stored elements, i.e. at most about
- * 1.07e9 elements.  The scratch array is about 1.02 MiB of device memory.
+ * 1.07e9 elements.  The scratch array is about 1.01 MiB of device memory.
  * Every device that loads the library holds it until the process exits.
  *
  * The first call on a device looks up the array's device address with that
  * device current.  Make that first call before any stream capture begins.
- * Later calls only enqueue work.  Every call on a device shares the one array:
+ * Later calls only enqueue work.  The address is cached per device together
+ * with the ID of the context it was found in; a call made in another context
+ * of that device (after cudaDeviceReset, say) looks it up again.  Concurrent
+ * first calls from several host threads are safe.  Every call on a device shares the one array:
  * calls whose work overlaps on the GPU (other streams, other host threads)
  * race and give wrong results.  Serialise them, e.g. on one stream.  Each call
  * clears the tickets it uses before its kernel runs.

@@ -38,7 +38,6 @@ MUON_DEBUG_KEEP_O = 1
 MUON_DEBUG_POISON_WORKSPACE = 2
 MUON_DEBUG_TIME_KERNELS = 4
 MUON_DEBUG_INJECT_LOST_LOAD = 8
-MUON_DEBUG_SINGLE_CTA_GEMM = 16
 
 KERNEL_KINDS = ("momentum_norm", "gram", "poly", "axpy", "axpy_update", "update", "axpy_o", "normuon")
 

@@ -15,7 +15,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 LIB_PATH = os.path.join(PKG_DIR, "libmuon.so")
-SOURCES = ["muon_api.cu", "momentum_norm.cu", "ns_gemm.cu", "ns_pair.cu", "noalloc.cu", "adamw.cu", "normuon.cu"]
+SOURCES = ["muon_api.cu", "momentum_norm.cu", "ns_pair.cu", "noalloc.cu", "adamw.cu", "normuon.cu"]
 HEADERS = ["kernels.cuh", "ptx.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

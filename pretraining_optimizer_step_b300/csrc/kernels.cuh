@@ -1,5 +1,5 @@
 // kernels.cuh -- launch parameters shared by the host planner (muon_api.cu) and
-// the device kernels (momentum_norm.cu, ns_gemm.cu).
+// the device kernels (momentum_norm.cu, ns_pair.cu, normuon.cu).
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -23,7 +23,7 @@ constexpr int kMomThreads = 256;
 struct MomentumMat {
     const float* g;
     float* mom;
-    float* p;             // published to p_table for the fused final update
+    float* p;             // weights (read by the standalone update only)
     __nv_bfloat16* x0;    // oriented X0 (unscaled u), m x n
     int rows, cols;       // stored shape
     int transposed;       // rows > cols: X0 = u^T
@@ -45,7 +45,6 @@ struct MomentumParams {
     unsigned int* counters;  // per step matrix; reset to 0 by the last CTA
     float* inv_norm;      // per step matrix: 1 / (||u|| + eps)
     float* norms;         // per step matrix: ||u||
-    float** p_table;      // per step matrix
 };
 
 // ------------------------------------------------------------------ weight update without NS
@@ -59,61 +58,23 @@ struct UpdateParams {
     float* const* dbg_O;  // per step matrix or nullptr
 };
 
-// ------------------------------------------------------------------ Newton-Schulz GEMM
-constexpr int kBM = 128;             // tile rows (TMEM lanes)
-constexpr int kBN = 256;             // tile columns (fp32 TMEM columns per accumulator)
-constexpr int kBK = 64;              // K slice per pipeline stage (128 B of bf16)
-constexpr int kStages = 4;
-constexpr int kAStageBytes = kBM * kBK * 2;   // 16 KiB
-constexpr int kBStageBytes = kBN * kBK * 2;   // 32 KiB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+// ------------------------------------------------------------------ Newton-Schulz GEMM tiling
+constexpr int kBM = 128;             // row block of the symmetric products (TMEM lanes per CTA)
+constexpr int kBN = 256;             // axpy column tile (fp32 TMEM columns per accumulator)
+constexpr int kBK = 64;              // K width of one 128B-swizzled operand panel (128 B of bf16)
 constexpr int kTmemCols = 512;       // two 256-column accumulators
 constexpr int kGemmThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 constexpr int kMaxClasses = 8;
 
-// Symmetric results (A, B) are computed on tiles on and above the diagonal.  ns_gemm_kernel
-// mirrors them below it; ns_pair_kernel stores the upper 128 x 128 blocks only and folds a I
-// into B, so its axpy modes compute s B' X with B' = B + a I.
+// Symmetric results (A, B) are computed on tiles on and above the diagonal and stored as
+// their upper 128 x 128 blocks; a I is folded into B, so the axpy modes compute s B' X with
+// B' = B + a I.
 enum GemmMode : int {
     MODE_GRAM = 0,        // A = s^2 X X^T
-    MODE_POLY = 1,        // B = b A + c A A
-    MODE_AXPY = 2,        // X' = s (a X + B X)
-    MODE_AXPY_FINAL = 3,  // O = s (a X + B X); p -= scale O
-    MODE_AXPY_O = 4,      // O = s (a X + B X) written in fp32 (stored layout) for the NorMuon pass
-};
-
-struct GemmClass {
-    int m, n;             // oriented X is m x n (m <= n)
-    int nmats;
-    int tile_begin;
-    int tiles_per_mat;
-    int k_blocks;         // ceil(K / 64)
-    int row_blocks;       // ceil(m / 128)
-    int col_tiles;        // axpy: ceil(n / 256)
-    int transposed;       // stored matrix is n x m
-    int mat_base;         // step index of the class's first matrix
-    const __nv_bfloat16* aux;  // poly: A ; axpy: X_in
-    __nv_bfloat16* out;        // gram: A ; poly: B ; axpy: X_out
-};
-
-struct GemmParams {
-    CUtensorMap tmA[kMaxClasses];  // M-side operand, K-major, box 64 x 128
-    CUtensorMap tmB[kMaxClasses];  // N-side operand: K-major box 64 x 128, or MN-major box 64 x 64 (axpy)
-    GemmClass cls[kMaxClasses];
-    int nclasses;
-    int total_tiles;
-    int mode;
-    int first_iter;       // fold 1/||u|| (X0 is stored unscaled)
-    float ca, cb, cc;
-    const float* inv_norm;     // per step matrix
-    const float* aspect;       // per step matrix: sqrt(max(1, rows/cols))
-    float lr;
-    float* const* p_table;     // per step matrix
-    float* const* dbg_O;       // per step matrix or nullptr
-    unsigned int* status;
-    unsigned long long timeout_ns;
-    int inject_lost_load;      // test hook (see MUON_DEBUG_INJECT_LOST_LOAD)
+    MODE_POLY = 1,        // B' = b A + c A A + a I
+    MODE_AXPY = 2,        // X' = s B' X
+    MODE_AXPY_FINAL = 3,  // O = s B' X; p -= scale O
+    MODE_AXPY_O = 4,      // O = s B' X written in fp32 (stored layout) for the NorMuon pass
 };
 
 // ------------------------------------------------------------------ NorMuon scaling
@@ -154,8 +115,6 @@ cudaError_t launch_normuon_update(const NormuonParams& p, cudaStream_t s);
 // Launchers (return the launch error, if any).
 cudaError_t launch_momentum_norm(const MomentumParams& p, cudaStream_t s);
 cudaError_t launch_update(const UpdateParams& p, cudaStream_t s);
-cudaError_t launch_ns_gemm(const GemmParams& p, int grid, cudaStream_t s);
-cudaError_t ns_gemm_prepare();  // one-time kernel attribute setup
 
 // ------------------------------------------------------------------ Newton-Schulz GEMM on CTA pairs
 // A cluster of two CTAs computes a 256 x N tile (N = 256, or 128 for a ragged
@@ -171,7 +130,6 @@ constexpr int kPairStageBytes = 4 * kPairPanelBytes;         // 64 KiB
 constexpr int kPairMaxStages = 3;
 // Shared memory by mode: Gram/poly/axpy use 3 stages + 8 KiB of epilogue slots per
 // warp; the final launch 2 stages + 24 KiB per warp (fp32 weight subtiles).
-constexpr int kEpiInSlotBytes = 6144;                        // fp32 32x32 (4 KiB) + bf16 32x32 (2 KiB)
 constexpr int kPairSmemBytes = 224 * 1024 + 1024;
 static_assert(3 * kPairStageBytes + 4 * 8192 <= 224 * 1024, "stage + epilogue layout");
 static_assert(2 * kPairStageBytes + 4 * 24576 <= 224 * 1024, "stage + epilogue layout (final)");

@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kMomThreads)
         const double nrm = sqrt(s);
         P.norms[M.gidx] = static_cast<float>(nrm);
         P.inv_norm[M.gidx] = static_cast<float>(1.0 / (nrm + static_cast<double>(P.eps)));
-        P.p_table[M.gidx] = M.p;
         P.counters[M.gidx] = 0u;
     }
 }

@@ -32,10 +32,11 @@ struct ClassPlan {
     __nv_bfloat16* X[2] = {nullptr, nullptr};
     __nv_bfloat16* A = nullptr;
     __nv_bfloat16* B = nullptr;
-    CUtensorMap tmXk[2], tmXmn[2], tmAk, tmBk;
-    // CTA-pair kernel: B-side K-major maps (box 64 x 64) and epilogue subtile maps (bf16 32 x 32)
+    // A-side K-major maps (box 64 x 128), B-side K-major maps (box 64 x 64), the MN-major X map
+    // of the axpy B operand (box 64 x 128), and epilogue subtile maps (bf16 32 x 32)
+    CUtensorMap tmXk[2], tmAk, tmBk;
     CUtensorMap tmXk64[2], tmAk64, tmXmn128[2], epiX[2], epiA, epiB;
-    int row_blocks = 0, col_tiles = 0, sym_tiles = 0, axpy_tiles = 0;
+    int row_blocks = 0, col_tiles = 0;
     int col_pairs = 0, sym_pair_tiles = 0, axpy_pair_tiles = 0;
 };
 
@@ -52,7 +53,6 @@ struct Plan {
     float* norms = nullptr;
     float* aspect = nullptr;
     unsigned int* counters = nullptr;
-    float** p_table = nullptr;
     float** dbg_table = nullptr;    // device array of per-matrix O buffers (KEEP_O)
     float* partials = nullptr;
     size_t workspace_bf16_bytes = 0;
@@ -170,17 +170,11 @@ double pair_axpy_exec_flops(int row_blocks, int n, int K) {
     return f;
 }
 
-int sym_tiles_per_mat(int row_blocks) {
-    int t = 0;
-    for (int bi = 0; bi < row_blocks; ++bi) t += (row_blocks - bi + 1) / 2;
-    return t;
-}
-
 // Host-only part of planning: shape classes, arena layout, tile counts.
 struct Layout {
     std::vector<size_t> offX0, offX1, offA, offB, off_dbg;
     size_t off_pmaps = 0, off_dmaps = 0;
-    size_t bf16_end = 0, off_inv = 0, off_nrm = 0, off_asp = 0, off_cnt = 0, off_pt = 0, off_dt = 0,
+    size_t bf16_end = 0, off_inv = 0, off_nrm = 0, off_asp = 0, off_cnt = 0, off_dt = 0,
            off_part = 0, total = 0;
     int momentum_ctas = 0;
     long long sym_tiles = 0, axpy_tiles = 0;
@@ -229,8 +223,6 @@ void compute_layout(Plan* P, const muon_shape* shapes, int n, bool keep_o, Layou
         L->offB.push_back(off); off = align_up(off + ab, 1024);
         cp.row_blocks = (cp.m + kBM - 1) / kBM;
         cp.col_tiles = (cp.n + kBN - 1) / kBN;
-        cp.sym_tiles = sym_tiles_per_mat(cp.row_blocks);
-        cp.axpy_tiles = cp.row_blocks * cp.col_tiles;
         cp.col_pairs = pair_col_pairs(cp.row_blocks);
         cp.sym_pair_tiles = pair_sym_tiles(cp.row_blocks);
         cp.axpy_pair_tiles = cp.col_pairs * cp.col_tiles;
@@ -248,7 +240,6 @@ void compute_layout(Plan* P, const muon_shape* shapes, int n, bool keep_o, Layou
     L->off_nrm = off; off = align_up(off + n * sizeof(float), 256);
     L->off_asp = off; off = align_up(off + n * sizeof(float), 256);
     L->off_cnt = off; off = align_up(off + n * sizeof(unsigned int), 256);
-    L->off_pt = off; off = align_up(off + n * sizeof(float*), 256);
     L->off_dt = off; off = align_up(off + n * sizeof(float*), 256);
     L->off_pmaps = off; off = align_up(off + n * sizeof(CUtensorMap), 256);
     L->off_dmaps = off; off = align_up(off + n * sizeof(CUtensorMap), 256);
@@ -304,7 +295,6 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
         muon_status st = MUON_OK;
         for (int pp = 0; pp < 2 && st == MUON_OK; ++pp) {
             st = encode_map(ctx->encode, &cp.tmXk[pp], cp.X[pp], cp.n, cp.m, G, kBK, kBM);
-            if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmXmn[pp], cp.X[pp], cp.n, cp.m, G, 64, kBK);
         }
         if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmAk, cp.A, cp.m, cp.m, G, kBK, kBM);
         if (st == MUON_OK) st = encode_map(ctx->encode, &cp.tmBk, cp.B, cp.m, cp.m, G, kBK, kBM);
@@ -334,7 +324,6 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
     P->norms = reinterpret_cast<float*>(a + L.off_nrm);
     P->aspect = reinterpret_cast<float*>(a + L.off_asp);
     P->counters = reinterpret_cast<unsigned int*>(a + L.off_cnt);
-    P->p_table = reinterpret_cast<float**>(a + L.off_pt);
     P->dbg_table = reinterpret_cast<float**>(a + L.off_dt);
     P->partials = reinterpret_cast<float*>(a + L.off_part);
 
@@ -598,7 +587,7 @@ muon_status muon_init(const muon_config* cfg) {
         return MUON_ERR_CUDA;
     }
     ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (ns_gemm_prepare() != cudaSuccess || ns_pair_prepare(&ctx->max_clusters) != cudaSuccess ||
+    if (ns_pair_prepare(&ctx->max_clusters) != cudaSuccess ||
         ctx->max_clusters < 1 ||
         cudaMalloc(&ctx->status, sizeof(unsigned int)) != cudaSuccess ||
         cudaMemset(ctx->status, 0, sizeof(unsigned int)) != cudaSuccess) {
@@ -681,7 +670,6 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
         mp.counters = P->counters;
         mp.inv_norm = P->inv_norm;
         mp.norms = P->norms;
-        mp.p_table = P->p_table;
         const muon_status st = timed_launch(ctx, 0, stream, [&] { return launch_momentum_norm(mp, stream); });
         if (st != MUON_OK) return st;
     }
@@ -711,7 +699,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
 
     // ---- Newton-Schulz iterations: per group of <= kMaxClasses classes
     const int nclass = static_cast<int>(P->classes.size());
-    if (!(ctx->debug & MUON_DEBUG_SINGLE_CTA_GEMM)) {
+    {
         // fp32 weight maps of the fused update: re-encoded only when the params change
         // (the NorMuon pass updates the weights in its own kernel)
         bool changed = false;
@@ -856,84 +844,6 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
         }
         return MUON_OK;
     }
-    // single-CTA kernel (MUON_DEBUG_SINGLE_CTA_GEMM): 128 x 256 tiles, one CTA per tile
-    static GemmParams gp;
-    for (int it = 0; it < ns_steps; ++it) {
-        const double* row = &ctx->coeffs[3 * it];
-        const int pin = it & 1, pout = pin ^ 1;
-        const bool last = (it == ns_steps - 1);
-        for (int g0 = 0; g0 < nclass; g0 += kMaxClasses) {
-            const int gc = std::min(kMaxClasses, nclass - g0);
-            for (int mode = MODE_GRAM; mode <= MODE_AXPY; ++mode) {
-                std::memset(&gp, 0, sizeof(gp));
-                const int eff_mode = (mode == MODE_AXPY && last) ? MODE_AXPY_FINAL : mode;
-                gp.mode = eff_mode;
-                gp.nclasses = gc;
-                gp.first_iter = (it == 0 && mode != MODE_POLY) ? 1 : 0;
-                gp.ca = static_cast<float>(row[0]);
-                gp.cb = static_cast<float>(row[1]);
-                gp.cc = static_cast<float>(row[2]);
-                gp.inv_norm = P->inv_norm;
-                gp.aspect = P->aspect;
-                gp.lr = lr;
-                gp.p_table = P->p_table;
-                gp.dbg_O = keep_o ? P->dbg_table : nullptr;
-                gp.status = ctx->status;
-                gp.timeout_ns = ctx->timeout_ns;
-                gp.inject_lost_load = ((ctx->debug & MUON_DEBUG_INJECT_LOST_LOAD) && !ctx->injected &&
-                                       it == 0 && mode == MODE_GRAM && g0 == 0)
-                                          ? 1
-                                          : 0;
-                if (gp.inject_lost_load) ctx->injected = true;
-                int tiles = 0;
-                int mat_base = 0;
-                for (int k = 0; k < g0; ++k) mat_base += static_cast<int>(P->classes[k].mats.size());
-                for (int k = 0; k < gc; ++k) {
-                    const ClassPlan& cp = P->classes[g0 + k];
-                    GemmClass& C = gp.cls[k];
-                    const int G = static_cast<int>(cp.mats.size());
-                    C.m = cp.m;
-                    C.n = cp.n;
-                    C.nmats = G;
-                    C.tile_begin = tiles;
-                    C.row_blocks = cp.row_blocks;
-                    C.col_tiles = cp.col_tiles;
-                    C.transposed = cp.transposed;
-                    C.mat_base = mat_base;
-                    if (mode == MODE_GRAM) {
-                        C.tiles_per_mat = cp.sym_tiles;
-                        C.k_blocks = (cp.n + kBK - 1) / kBK;
-                        C.aux = nullptr;
-                        C.out = cp.A;
-                        gp.tmA[k] = cp.tmXk[pin];
-                        gp.tmB[k] = cp.tmXk[pin];
-                    } else if (mode == MODE_POLY) {
-                        C.tiles_per_mat = cp.sym_tiles;
-                        C.k_blocks = (cp.m + kBK - 1) / kBK;
-                        C.aux = cp.A;
-                        C.out = cp.B;
-                        gp.tmA[k] = cp.tmAk;
-                        gp.tmB[k] = cp.tmAk;
-                    } else {
-                        C.tiles_per_mat = cp.axpy_tiles;
-                        C.k_blocks = (cp.m + kBK - 1) / kBK;
-                        C.aux = cp.X[pin];
-                        C.out = cp.X[pout];
-                        gp.tmA[k] = cp.tmBk;
-                        gp.tmB[k] = cp.tmXmn[pin];
-                    }
-                    tiles += C.tiles_per_mat * G;
-                    mat_base += G;
-                }
-                gp.total_tiles = tiles;
-                const int grid = std::min(tiles, ctx->sm_count);
-                const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3 : 4;
-                const muon_status st = timed_launch(ctx, kind, stream, [&] { return launch_ns_gemm(gp, grid, stream); });
-                if (st != MUON_OK) return st;
-            }
-        }
-    }
-    return MUON_OK;
 }
 
 muon_status muon_step(float* const params[], const float* const grads[], float* const momentum_bufs[],
@@ -951,7 +861,7 @@ muon_status muon_step_normuon(float* const params[], const float* const grads[],
     if (n_mats < 0) return MUON_ERR_INVALID_ARG;
     if (n_mats == 0) return step_impl(params, grads, momentum_bufs, shapes, 0, lr, beta, nesterov, ns_steps, stream,
                                       nullptr);
-    if (!second_moments || ns_steps < 1 || (ctx->debug & MUON_DEBUG_SINGLE_CTA_GEMM)) return MUON_ERR_INVALID_ARG;
+    if (!second_moments || ns_steps < 1) return MUON_ERR_INVALID_ARG;
     if (!(beta2 >= 0.0f && beta2 < 1.0f) || !(eps2 >= 0.0f) || !std::isfinite(eps2)) return MUON_ERR_INVALID_ARG;
     for (int i = 0; i < n_mats; ++i) {
         if (!second_moments[i]) return MUON_ERR_INVALID_ARG;

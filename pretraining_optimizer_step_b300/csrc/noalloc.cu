@@ -7,10 +7,10 @@
 //   partials  kNoAllocMaxTiles floats   one fp32 sum of squares per CTA (64 x 64 tile)
 //   tickets   kNoAllocMaxMats  uint32   per-matrix arrival counters (must start at 0)
 //   inv_norm  kNoAllocMaxMats  floats   1/(||u|| + eps), written by the kernel
-//   p_table   kNoAllocMaxMats  pointers written by the kernel (unused here)
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/muon.h"
 #include "kernels.cuh"
@@ -26,18 +26,54 @@ constexpr int kNoAllocMaxDevices = 64;
 constexpr size_t kOffPartials = 0;
 constexpr size_t kOffTickets = kOffPartials + sizeof(float) * kNoAllocMaxTiles;
 constexpr size_t kOffInvNorm = kOffTickets + sizeof(unsigned int) * kNoAllocMaxMats;
-constexpr size_t kOffPTable = kOffInvNorm + sizeof(float) * kNoAllocMaxMats;
-constexpr size_t kScratchBytes = kOffPTable + sizeof(float*) * kNoAllocMaxMats;
-static_assert(kOffTickets % 256 == 0 && kOffInvNorm % 256 == 0 && kOffPTable % 256 == 0,
-              "scratch sections stay 256-byte aligned");
+constexpr size_t kScratchBytes = kOffInvNorm + sizeof(float) * kNoAllocMaxMats;
+static_assert(kOffTickets % 256 == 0 && kOffInvNorm % 256 == 0, "scratch sections stay 256-byte aligned");
 
 // The fixed scratch.  In host code this name is only a stand-in for the
 // symbol, not a device address: the address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch per device ordinal, looked up by the
-// first call on that device (nullptr until then).
-unsigned char* g_scratch_addr[kNoAllocMaxDevices] = {};
+// first call on that device, together with the ID of the context it belongs
+// to.  A call whose current context has another ID (cudaDeviceReset ends a
+// context; the next one may load the module elsewhere) looks it up again.
+// The mutex makes concurrent first calls from several host threads safe.
+struct ScratchSlot {
+    unsigned char* addr = nullptr;
+    unsigned long long ctx_id = 0;
+};
+ScratchSlot g_scratch[kNoAllocMaxDevices];
+std::mutex g_scratch_mutex;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// ID of the calling thread's current context (0 when none is current or the
+// driver does not offer the query).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();
+        resolved = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+        get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
 
 muon_status scratch_for_current_device(unsigned char** out) {
     int dev = -1;
@@ -46,22 +82,28 @@ muon_status scratch_for_current_device(unsigned char** out) {
         return MUON_ERR_UNSUPPORTED_DEVICE;
     }
     if (dev >= kNoAllocMaxDevices) return MUON_ERR_UNSUPPORTED_DEVICE;
-    if (g_scratch_addr[dev] == nullptr) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return MUON_ERR_UNSUPPORTED_DEVICE;
-        }
-        if (!(major == 10 && minor == 3)) return MUON_ERR_UNSUPPORTED_DEVICE;
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
-            cudaGetLastError();
-            return MUON_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = static_cast<unsigned char*>(ptr);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    ScratchSlot& slot = g_scratch[dev];
+    if (slot.addr != nullptr && slot.ctx_id != 0 && slot.ctx_id == current_context_id()) {
+        *out = slot.addr;
+        return MUON_OK;
     }
-    *out = g_scratch_addr[dev];
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MUON_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (!(major == 10 && minor == 3)) return MUON_ERR_UNSUPPORTED_DEVICE;
+    // with this device current: the symbol's address in its (primary) context
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return MUON_ERR_CUDA;
+    }
+    slot.addr = static_cast<unsigned char*>(ptr);
+    slot.ctx_id = current_context_id();  // 0 (unknown) makes the next call look it up again
+    *out = slot.addr;
     return MUON_OK;
 }
 
@@ -146,7 +188,6 @@ extern "C" muon_status muon_momentum_norm_noalloc(const float* const grads[], fl
         mp.counters = tickets;
         mp.inv_norm = reinterpret_cast<float*>(scratch + kOffInvNorm);
         mp.norms = norms_out;
-        mp.p_table = reinterpret_cast<float**>(scratch + kOffPTable);
         if (launch_momentum_norm(mp, stream) != cudaSuccess) return MUON_ERR_CUDA;
     }
     return MUON_OK;

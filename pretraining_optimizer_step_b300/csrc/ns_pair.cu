@@ -3,8 +3,7 @@
 // One iteration of the quintic loop ("Cara Melatih ChatGPT Sendiri dengan
 // Budget 50 Dolar", section "2. Pengoptimal Muon", orthogonalization loop) is
 // three launches of this kernel over every matrix of the step (grouped by
-// oriented shape class); the modes and their epilogues are those of
-// ns_gemm.cu:
+// oriented shape class), one per mode:
 //   MODE_GRAM        A = s^2 X X^T               tiles on/above the diagonal, upper blocks stored
 //   MODE_POLY        B' = b A + c A A + a I      A symmetric: A A = A A^T, same operand both sides
 //   MODE_AXPY        X' = s B' X                 X read MN-major as the B operand
