@@ -31,13 +31,13 @@ def test_lost_load_times_out_and_the_context_survives():
     finally:
         mu.muon_destroy()
     # a fresh context on the same device computes a correct step
-    mu.muon_init(debug_flags=mu.MUON_DEBUG_KEEP_O, wait_timeout_s=2.0)
+    mu.muon_init(wait_timeout_s=2.0)
     try:
         p, g, m, _ = workloads.make_stack("d2", "cuda")
         p0, g0, m0 = ([t.cpu().numpy().copy() for t in ts] for ts in (p, g, m))
-        O = run_gpu_step(p, g, m)
+        run_gpu_step(p, g, m)
         for i in (0, 4, 5):
-            check_matrix(i, p0[i], g0[i], m0[i], p[i].cpu().numpy(), m[i].cpu().numpy(), O[i], 0.02, 0.95, True, 5,
+            check_matrix(i, p0[i], g0[i], m0[i], p[i].cpu().numpy(), m[i].cpu().numpy(), None, 0.02, 0.95, True, 5,
                          oracle.DEFAULT_COEFFS)
     finally:
         mu.muon_destroy()

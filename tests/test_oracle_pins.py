@@ -156,11 +156,47 @@ def check_momentum():
     # Nesterov: u = g + beta m'
     mo, u = oracle.momentum(g, m, 0.9, True)
     assert np.allclose(u, g64 + 0.9 * (0.9 * m64 + g64), rtol=0, atol=1e-12)
-    # EMA form: m' = beta m + (1-beta) g ; u = (1-beta) g + beta m'
-    mo, u = oracle.momentum(g, m, 0.75, True, mode=1)
-    mn = 0.75 * m64 + 0.25 * g64
-    assert np.allclose(mo, mn, rtol=1e-6, atol=1e-7)
-    assert np.allclose(u, 0.25 * g64 + 0.75 * mn, rtol=0, atol=1e-12)
+
+
+def _constant_gradient_run(g, beta, mode, nesterov, steps):
+    """Momentum states m_1..m_k and directions u_0..u_{k-1} from m_0 = 0 under a constant g."""
+    m = np.zeros_like(g)
+    ms, us = [], []
+    for _ in range(steps):
+        m, u = oracle.momentum(g, m, beta, nesterov, mode=mode)
+        ms.append(m.astype(np.float64))
+        us.append(u)
+    return ms, us
+
+
+def check_momentum_transients():
+    # Facts about both momentum forms that do not restate their update rule:
+    #  * from m = 0 under a constant gradient g, the heavy-ball buffer is the partial geometric
+    #    sum m_k = g (1 - beta^k) / (1 - beta), and the EMA buffer is its (1 - beta)-weighted
+    #    form m_k = g (1 - beta^k) (the bias the usual EMA correction divides out);
+    #  * Nesterov looks one step ahead: under a constant gradient the direction of step k is the
+    #    buffer the next step will hold, u_k = m_{k+1} (plain momentum: u_k = m_k);
+    #  * the EMA buffer started at m = g stays at g, and beta = 0 gives m' = u = g.
+    rng = np.random.default_rng(8)
+    g = rng.standard_normal((3, 8)).astype(np.float32)
+    g64 = g.astype(np.float64)
+    beta = 0.9
+    steps = 6
+    for mode in (0, 1):
+        for nesterov in (False, True):
+            ms, us = _constant_gradient_run(g, beta, mode, nesterov, steps + 1)
+            for k in range(1, steps + 1):
+                geo = (1.0 - beta ** k) / (1.0 - beta)
+                expect = g64 * (geo if mode == 0 else (1.0 - beta ** k))
+                assert np.allclose(ms[k - 1], expect, rtol=1e-6, atol=1e-7), (mode, nesterov, k)
+            for k in range(steps):
+                ahead = ms[k + 1] if nesterov else ms[k]
+                assert np.allclose(us[k], ahead, rtol=1e-6, atol=1e-7), (mode, nesterov, k)
+    for nesterov in (False, True):
+        mo, u = oracle.momentum(g, g.copy(), 0.75, nesterov, mode=1)
+        assert np.allclose(mo, g64, rtol=1e-7, atol=0) and np.allclose(u, g64, rtol=1e-7, atol=0)
+        mo, u = oracle.momentum(g, rng.standard_normal(g.shape).astype(np.float32), 0.0, nesterov, mode=1)
+        assert np.array_equal(mo, g) and np.allclose(u, g64, rtol=0, atol=0)
 
 
 def check_update_scale():
@@ -178,7 +214,7 @@ def check_update_scale():
 
 PIN_CHECKS = [check_closed_form, check_closed_form_nonnormal_square, check_band,
               check_orthogonal_input, check_hand_iteration, check_row_vector,
-              check_orientation_and_scale, check_momentum, check_update_scale]
+              check_orientation_and_scale, check_momentum, check_momentum_transients, check_update_scale]
 
 
 @pytest.mark.parametrize("check", PIN_CHECKS, ids=lambda f: f.__name__)
@@ -213,6 +249,10 @@ MUTANTS = {
     "aspect_inverted": ("(double)r / (double)c", "(double)c / (double)r"),
     "nesterov_uses_old_m": ("u = nesterov ? gd + beta * mn : mn", "u = nesterov ? gd + beta * md : mn"),
     "momentum_no_beta": ("mn = beta * md + gd", "mn = md + gd"),
+    "ema_no_one_minus_beta": ("mn = beta * md + (1.0 - beta) * gd", "mn = beta * md + gd"),
+    "ema_weights_swapped": ("mn = beta * md + (1.0 - beta) * gd", "mn = (1.0 - beta) * md + beta * gd"),
+    "ema_nesterov_uses_old_m": ("u = nesterov ? (1.0 - beta) * gd + beta * mn : mn",
+                                "u = nesterov ? (1.0 - beta) * gd + beta * md : mn"),
     "loop_one_short": ("for (int k = 0; k < K; ++k)", "for (int k = 1; k < K; ++k)"),
 }
 
