@@ -28,7 +28,7 @@ import torch
 import oracle
 import pretraining_optimizer_step_b300 as mu
 import workloads
-from gpu_util import check_momentum, o_from_update, rel_fro
+from gpu_util import check_momentum, o_from_update, rel_fro, update_scale
 
 pytestmark = pytest.mark.gpu
 
@@ -85,9 +85,13 @@ def _run_two_calls(name, shapes, p, g, m, check_oracle_idx):
             assert abs(got_norms[i] - ref) <= 1e-6 * ref, (call, i, got_norms[i], ref)
             x = _oriented_back(x0[i], s)
             O_na = x / (float(got_norms[i]) + EPS)
-            O_step = o_from_update(p0[i], p[i].cpu().numpy(), 0.02, s)
+            p1 = p[i].cpu().numpy()
+            O_step = o_from_update(p0[i], p1, 0.02, s)
+            # O recovered from p' = p - sc O carries p''s float32 rounding (at most 2^-24 |p'| per
+            # entry) divided by sc; at ns_steps = 0, ||O||_F is 1, so that is a few 1e-5 here
+            bound = 2.0 ** -23 * np.linalg.norm(p1) / (float(update_scale(0.02, s)) * np.linalg.norm(O_step)) + 1e-6
             err = rel_fro(O_na, O_step)
-            assert err <= 1e-5, (call, i, err)
+            assert err <= bound, (call, i, err, bound)
             if i in check_oracle_idx:
                 _check_against_oracle(i, g0[i], m0[i], m_na[i].cpu().numpy(), x, float(got_norms[i]))
 
