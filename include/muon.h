@@ -22,7 +22,8 @@
  * Precision: p, g, m are float32 (fp32 state); the Newton-Schulz operands X, A,
  * B are stored as bfloat16 (round to nearest even) and every product
  * accumulates in fp32; the last iteration's result O is formed in fp32 and
- * applied to p without being stored.
+ * applied to p without being stored: p' = p + fp32(-lr sqrt(max(1, rows/cols)) O),
+ * the addition made in fp32 by the memory system (a TMA reduce-add).
  *
  * Conventions shared by every entry point:
  *  - All functions return a muon_status; none aborts, throws or prints.

@@ -128,11 +128,11 @@ constexpr int kPairBK = 128;
 constexpr int kPairPanelBytes = 128 * 64 * 2;               // 16 KiB
 constexpr int kPairStageBytes = 4 * kPairPanelBytes;         // 64 KiB
 constexpr int kPairMaxStages = 3;
-// Shared memory by mode: Gram/poly/axpy use 3 stages + 8 KiB of epilogue slots per
-// warp; the final launch 2 stages + 24 KiB per warp (fp32 weight subtiles).
+// Shared memory by mode: every launch uses 3 stages + 8 KiB of epilogue slots per warp,
+// except a final launch that also stores the debug copy of O: 2 stages + 24 KiB per warp.
 constexpr int kPairSmemBytes = 224 * 1024 + 1024;
 static_assert(3 * kPairStageBytes + 4 * 8192 <= 224 * 1024, "stage + epilogue layout");
-static_assert(2 * kPairStageBytes + 4 * 24576 <= 224 * 1024, "stage + epilogue layout (final)");
+static_assert(2 * kPairStageBytes + 4 * 24576 <= 224 * 1024, "stage + epilogue layout (final, debug O)");
 
 struct PairClass {
     int m, n;             // oriented X is m x n (m <= n)

@@ -7,11 +7,13 @@
 //   MODE_GRAM        A = s^2 X X^T               tiles on/above the diagonal, upper blocks stored
 //   MODE_POLY        B' = b A + c A A + a I      A symmetric: A A = A A^T, same operand both sides
 //   MODE_AXPY        X' = s B' X                 X read MN-major as the B operand
-//   MODE_AXPY_FINAL  O = s B' X in fp32, p -= lr sqrt(max(1, r/c)) O
+//   MODE_AXPY_FINAL  O = s B' X in fp32, p += -lr sqrt(max(1, r/c)) O (TMA reduce-add)
 //   MODE_AXPY_O      O = s B' X in fp32, stored (stored layout) for the NorMuon pass
 // Folding a I into the polynomial makes a X + B X = (B + a I) X a plain product, so the
-// axpy epilogues read nothing but the accumulator (and the weights in the final launch);
-// the only numerical change is one bf16 rounding of B's diagonal entries plus a.
+// axpy epilogues read nothing but the accumulator; the only numerical change is one bf16
+// rounding of B's diagonal entries plus a.  The final launch never reads the weights: it
+// writes the fp32 weight change -lr s O to shared memory and a TMA reduce-add folds it into
+// p in L2 (p' = p + fp32(-lr s O)).
 //
 // A cluster of two CTAs (one per SM) computes a 256 x N tile with
 // tcgen05.mma.cta_group::2: CTA rank r holds rows [128 r, 128 r + 128) of the A
@@ -33,16 +35,18 @@
 //   axpy:      tile = row blocks (2 rp, 2 rp + 1) x columns [256 ct, 256 ct + N).
 //
 // CTA layout (192 threads, persistent over the pair tiles):
-//   warp 0      TMA producer (both CTAs): ring of 3 stages (2 in the final launch) of
+//   warp 0      TMA producer (both CTAs): ring of 3 stages (2 in the final launch when it
+//               also stores the debug copy of O) of
 //               {A 128 x 128, B-half <= 128 x 128} bf16 as 64-wide K panels; the loads
 //               of both CTAs complete on the even CTA's mbarrier
 //   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues 8 MMAs
 //               (M 256, N 256/128, K 16) per stage and commits to both CTAs' barriers
 //   warps 2..5  epilogue (both CTAs): per warp 32 rows, in chunks of 32 columns.
-//               Inputs (the A or X tile; the fp32 weights in the final launch)
-//               arrive by TMA into a ring of swizzled shared slots, one chunk
-//               ahead (two in the final launch); outputs leave by TMA store from
-//               swizzled slots.  Threads touch shared memory only
+//               The polynomial's input (the A tile) arrives by TMA into a ring of
+//               swizzled shared slots, one chunk ahead; outputs leave by TMA store
+//               (reduce-add for the weights) from a ring of swizzled slots, and a
+//               slot is rewritten only once the store that last read it has read
+//               it (one bulk group per chunk).  Threads touch shared memory only
 //               with conflict-free 16-byte vectors (row access) or 4-byte/2-byte
 //               column access (transposes).
 // Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, raises its
@@ -134,8 +138,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const uint32_t tiles_base = (raw + 1023u) & ~1023u;
     uint8_t* tiles_ptr = smem_raw + (tiles_base - raw);
     const bool final_mode = P.mode == MODE_AXPY_FINAL;
-    const int nstages = final_mode ? 2 : 3;
-    const int epi_warp_bytes = final_mode ? 24576 : 8192;
+    const bool dbg_o = final_mode && P.dbg_maps != nullptr;   // debug copy of O in the final launch
+    const int nstages = dbg_o ? 2 : 3;
+    const int epi_warp_bytes = dbg_o ? 24576 : 8192;
     uint8_t* epi_ptr = tiles_ptr + nstages * kPairStageBytes;
 
     const int warp = threadIdx.x >> 5;
@@ -304,22 +309,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int lg = warp & 3;                       // TMEM lane group of this warp
         uint8_t* wbase = epi_ptr + lg * epi_warp_bytes;
-        const bool has_in = P.mode == MODE_POLY || final_mode;
+        const bool has_in = P.mode == MODE_POLY;
         // The warp's epilogue slots, by mode (an input slot holds chunk c when c % n_in == slot;
-        // loads run n_in - 1 chunks ahead; output slots alternate per committed store group):
-        //   final (24 KiB): 4 input slots of fp32 32x32 weights (4 KiB) + 1 output slot (fp32 O,
-        //                   for the debug copy)
-        //   gram  (8 KiB):  4 output slots of bf16
-        //   poly  (8 KiB):  2 bf16 input slots (A) + 2 output slots of bf16
-        //   axpy  (8 KiB):  4 output slots of bf16
-        //   axpy_o (8 KiB): 2 output slots of fp32 O
+        // loads run n_in - 1 chunks ahead; output slots alternate per committed store group, and
+        // a slot is rewritten once the group that last read it -- n_out groups back -- has):
+        //   final (8 KiB):   2 output slots of the fp32 32x32 weight change -lr s O
+        //   final, debug copy of O (24 KiB): 2 output slot pairs {weight change, O} of 8 KiB
+        //   gram  (8 KiB):   4 output slots of bf16
+        //   poly  (8 KiB):   2 bf16 input slots (A) + 2 output slots of bf16
+        //   axpy  (8 KiB):   4 output slots of bf16
+        //   axpy_o (8 KiB):  2 output slots of fp32 O
         const bool o_mode = P.mode == MODE_AXPY_O;
-        const int n_in = final_mode ? 4 : (has_in ? 2 : 0);
-        const int in_stride = final_mode ? 4096 : 2048;
-        const int n_out = final_mode ? 1 : (o_mode || P.mode == MODE_POLY) ? 2 : 4;
-        const int out_stride = (final_mode || o_mode) ? 4096 : 2048;
+        const bool f32_out = final_mode || o_mode;
+        const int n_in = has_in ? 2 : 0;
+        const int in_stride = 2048;
+        const int n_out = (f32_out || P.mode == MODE_POLY) ? 2 : 4;
+        const int out_stride = dbg_o ? 8192 : (f32_out ? 4096 : 2048);
         uint8_t* out_base = wbase + n_in * in_stride;
-        auto in_f32 = [&](int sl) { return wbase + sl * in_stride; };
         auto in_b16 = [&](int sl) { return wbase + sl * in_stride; };
         uint64_t* ibar = in_bar[lg];
         uint32_t in_phase_bits = 0u, in_pending_bits = 0u;
@@ -347,23 +353,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 if (sym && (cc0 >> 7) < pt.rb) return false;
                 return true;
             };
-            auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0
+            auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0 (polynomial: the A tile)
                 const int slot = ch % n_in;
                 const int cc0 = pt.c0 + ch * 32;
-                if (final_mode) {
-                    mbar_arrive_expect_tx(&ibar[slot], 4096u);
-                    if (transposed) tma_load_2d(in_f32(slot), pmap, &ibar[slot], grow0, cc0);
-                    else tma_load_2d(in_f32(slot), pmap, &ibar[slot], cc0, grow0);
-                } else {
-                    mbar_arrive_expect_tx(&ibar[slot], 2048u);
-                    tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
-                }
+                mbar_arrive_expect_tx(&ibar[slot], 2048u);
+                tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 in_pending_bits |= 1u << slot;
             };
             if (has_in && lane == 0) {
-                // the final launch stores the updated weights from these slots: the previous
-                // tile's stores must have read them before the new loads land
-                if (final_mode) bulk_wait_group_read0();
                 for (int ch = 0; ch < n_in && ch < nch; ++ch)
                     if (live(ch)) issue_in(ch);
             }
@@ -433,47 +430,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] *= s;
                     }
-                    // the output slot about to be written must no longer be read by an earlier store
-                    // (final: the single slot; others: the slot of the group before the last)
+                    // the output slot about to be written must no longer be read by the store group
+                    // that last used it, n_out groups back (the most recent n_out - 1 may still read)
                     if (lane == 0) {
-                        if (n_out == 1) bulk_wait_group_read0();
-                        else if (n_out == 2) bulk_wait_group_read1();
+                        if (n_out == 2) bulk_wait_group_read1();
                         else bulk_wait_group_read3();
                     }
                     __syncwarp();
                     uint8_t* out_slot = out_base + (groups % static_cast<uint32_t>(n_out)) * out_stride;
                     if (final_mode) {
-                        // p -= sc O on the fp32 weight subtile, in place
-                        uint8_t* pf = in_f32(slot);
+                        // the fp32 weight change -sc O in the stored layout (rows = stored rows);
+                        // a transposed subtile has stored rows = oriented columns j, columns = lanes
                         if (!transposed) {
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                float4* q = reinterpret_cast<float4*>(pf + sw128_unit(lane, u));
-                                float4 w = *q;
-                                w.x = fmaf(-sc, v[4 * u + 0], w.x);
-                                w.y = fmaf(-sc, v[4 * u + 1], w.y);
-                                w.z = fmaf(-sc, v[4 * u + 2], w.z);
-                                w.w = fmaf(-sc, v[4 * u + 3], w.w);
-                                *q = w;
-                            }
+                            for (int u = 0; u < 8; ++u)
+                                *reinterpret_cast<float4*>(out_slot + sw128_unit(lane, u)) =
+                                    make_float4(-sc * v[4 * u], -sc * v[4 * u + 1], -sc * v[4 * u + 2],
+                                                -sc * v[4 * u + 3]);
                         } else {
-                            // subtile rows are stored rows (= oriented columns j), columns are lanes
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                float* q = reinterpret_cast<float*>(pf + sw128_elem(j, lane));
-                                *q = fmaf(-sc, v[j], *q);
-                            }
+                            for (int j = 0; j < 32; ++j)
+                                *reinterpret_cast<float*>(out_slot + sw128_elem(j, lane)) = -sc * v[j];
                         }
-                        if (P.dbg_maps) {
+                        if (dbg_o) {
+                            uint8_t* o_slot = out_slot + 4096;
                             if (!transposed) {
 #pragma unroll
                                 for (int u = 0; u < 8; ++u)
-                                    *reinterpret_cast<float4*>(out_slot + sw128_unit(lane, u)) =
+                                    *reinterpret_cast<float4*>(o_slot + sw128_unit(lane, u)) =
                                         make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)
-                                    *reinterpret_cast<float*>(out_slot + sw128_elem(j, lane)) = v[j];
+                                    *reinterpret_cast<float*>(o_slot + sw128_elem(j, lane)) = v[j];
                             }
                         }
                     } else if (o_mode) {
@@ -503,11 +492,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         if (final_mode) {
-                            if (transposed) tma_store_2d(pmap, in_f32(slot), grow0, cc0);
-                            else tma_store_2d(pmap, in_f32(slot), cc0, grow0);
-                            if (P.dbg_maps) {
-                                if (transposed) tma_store_2d(&P.dbg_maps[gm], out_slot, grow0, cc0);
-                                else tma_store_2d(&P.dbg_maps[gm], out_slot, cc0, grow0);
+                            if (transposed) tma_reduce_add_2d(pmap, out_slot, grow0, cc0);
+                            else tma_reduce_add_2d(pmap, out_slot, cc0, grow0);
+                            if (dbg_o) {
+                                if (transposed) tma_store_2d(&P.dbg_maps[gm], out_slot + 4096, grow0, cc0);
+                                else tma_store_2d(&P.dbg_maps[gm], out_slot + 4096, cc0, grow0);
                             }
                         } else if (o_mode) {
                             if (transposed) tma_store_2d(&P.o_maps[gm], out_slot, grow0, cc0);
@@ -521,10 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     ++groups;  // every lane keeps the count (warp-uniform)
                 }
                 // refill this slot with the chunk n_in ahead
-                if (has_in && lane == 0 && ch + n_in < nch && live(ch + n_in)) {
-                    if (final_mode) bulk_wait_group_read0();  // the p store above reads this slot
-                    issue_in(ch + n_in);
-                }
+                if (has_in && lane == 0 && ch + n_in < nch && live(ch + n_in)) issue_in(ch + n_in);
             }
             if (failed) break;
             if (++acc == 2) {

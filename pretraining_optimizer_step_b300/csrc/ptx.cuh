@@ -204,6 +204,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                  "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                  : "memory");
 }
+// Tiled element-wise add of a shared-memory box into global memory (the element type is the
+// tensor map's; the read-modify-write happens in L2).  Same completion mechanism as the stores.
+// Coordinates must be non-negative; the innermost one times the element size a multiple of 16 B.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk group has finished reading its shared memory source.
 __device__ __forceinline__ void bulk_wait_group_read0() {
