@@ -39,6 +39,21 @@ MUON_DEBUG_POISON_WORKSPACE = 2
 MUON_DEBUG_TIME_KERNELS = 4
 MUON_DEBUG_INJECT_LOST_LOAD = 8
 
+# The five per-iteration "Polar Express" (a, b, c) rows, for muon_init(coeffs=...).  The pages
+# print the first two to three decimals (apidog.com "Cara Melatih ChatGPT Sendiri dengan Budget 50
+# Dolar", section "2. Pengoptimal Muon", coefficient list) and elide the rest; these full-precision
+# rows come from the Polar Express construction (greedy minimax odd quintics on the interval where
+# the singular values lie: start 1e-3, cushion u/50, recentring on 1, safety factor 1.02 on every
+# row but the last), and agree with the printed figures to their last decimal.  The default table
+# stays the fixed quintic (3.4445, -4.7750, 2.0315) x 5.
+POLAR_EXPRESS_COEFFS = (
+    (8.156554524902461, -22.483292925577953, 15.878769915207466),
+    (4.042929935166726, -2.8089174659087055, 0.50001784510513),
+    (3.891667802292667, -2.772484153217687, 0.5060648178503395),
+    (3.2857536577556523, -2.3681294933425345, 0.4644902423300303),
+    (2.3465413258596395, -1.7097828382687077, 0.4232355116930525),
+)
+
 KERNEL_KINDS = ("momentum_norm", "gram", "poly", "axpy", "axpy_update", "update", "axpy_o", "normuon")
 
 

@@ -107,6 +107,21 @@ def test_pages_polar_express_rows():
     run_and_check(p, g, m, coeffs=np.array(rows), ns_steps=2)
 
 
+@pytest.mark.parametrize("case", ["d2", "ragged"])
+def test_derived_polar_express_table(case):
+    # the full five-row table of the Polar Express construction (the two rows the pages print
+    # and the three derived ones; tests/test_polar_express.py pins it on the CPU).  A model of
+    # the kernels' rounding gives O errors of 1.3e-2 to 1.7e-2 with it on the d2 shapes
+    rows = [tuple(r) for r in mu.POLAR_EXPRESS_COEFFS]
+    mu.muon_destroy()
+    mu.muon_init(coeffs=rows, wait_timeout_s=2.0)
+    if case == "d2":
+        p, g, m, _ = workloads.make_stack("d2", "cuda")
+    else:
+        p, g, m, _ = workloads.make_custom(RAGGED, "cuda", tag="ragged")
+    run_and_check(p, g, m, coeffs=np.array(rows), ns_steps=5, tol_o=small_side_tol)
+
+
 def test_per_iteration_rows_switch():
     # five iterations whose rows alternate between the default quintic and the
     # cubic Newton-Schulz step X <- 1.5 X - 0.5 X X^T X (a, b, c = 1.5, -0.5, 0):
