@@ -5,8 +5,9 @@ attention matrices, the 6656 x 1664 MLP input and the 1664 x 6656 MLP output
 (156 fp32 matrices, 8.64e8 elements) -- one Muon step per timed step: Nesterov
 momentum (beta 0.95), Frobenius normalisation, 5 quintic Newton-Schulz
 iterations, aspect-scaled update (lr 0.02).  Consecutive steps carry the
-momentum and weights and read the next of four pre-drawn gradient sets (each
-3.46 GB, far above the 126 MB L2, so no flush is needed between steps).
+momentum and weights, and every step reads a gradient set of its own, drawn on
+the device before the timed region (3.46 GB each, far above the 126 MB L2, so
+no flush is needed between steps; past 32 steps the sets are reused in turn).
 
 Metric: algorithmic Newton-Schulz TFLOP/s of the whole step (3 m^2 n + m^3 per
 matrix and iteration, m <= n the oriented sides) = flops / step time; the line
@@ -45,6 +46,8 @@ def workload_desc(name):
     return (f"{name}: {len(shapes)} fp32 matrices of shapes {kinds}, Nesterov beta 0.95, lr 0.02, "
             "5 Newton-Schulz iterations")
 
+
+MAX_GRAD_SETS = 32  # past this many steps the pre-drawn gradient sets are reused in turn
 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -169,20 +172,34 @@ class ClockSampler:
                 "power_w_max": max(self.power) if self.power else None, "source": self.source}
 
 
+# DRAM bytes (read + write) per Newton-Schulz launch at d26, from one ncu capture of the
+# d26x2 workload (the same shapes, 2 of the 26 layers) scaled by 13, and the sha256 of the
+# kernel source it was taken on.  The figure is reported only while the source is unchanged.
+NS_PAIR_TRAFFIC = {"bytes_per_launch_d26": None, "source_sha256": None}
+
+
 def ns_pair_traffic():
-    """DRAM bytes per NS launch at d26 from the committed ncu summary, or None when the
-    kernel source changed since that capture (the summary records its sha256)."""
+    """DRAM bytes per NS launch at d26, or None when the kernel changed since the capture."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "ns_pair_d26x2_full.md")
     src = os.path.join(ROOT, "pretraining_optimizer_step_b300", "csrc", "ns_pair.cu")
     try:
-        fields = dict(ln.split(": ", 1) for ln in open(path).read().splitlines() if ": " in ln
-                      and ln.split(": ", 1)[0] in ("source_sha256", "bytes_per_launch_d26"))
-        if fields.get("source_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
-            return None
-        return float(fields["bytes_per_launch_d26"])
-    except (OSError, ValueError, KeyError):
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
         return None
+    if NS_PAIR_TRAFFIC["source_sha256"] != digest:
+        return None
+    return NS_PAIR_TRAFFIC["bytes_per_launch_d26"]
+
+
+def cpu_model() -> str:
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
 
 
 # ---------------------------------------------------------------- multi-rank host logic
@@ -203,10 +220,16 @@ def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> fl
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def oracle_sample(idx=(0, 4), workload=WORKLOAD):
-    """Time the fp64 oracle on a bounded sample of the workload: one full Muon
-    step of the listed matrices (for d26: 0 is 1664 x 1664, 4 is 6656 x 1664).
-    Returns (TFLOP/s of algorithmic NS flops, seconds, description, threads, flops)."""
+def default_sample(workload):
+    """Matrices of the oracle's timed sample: for the stacks a square attention matrix and the
+    4:1 MLP input (for d26: 0 is 1664 x 1664, 4 is 6656 x 1664), else the first matrix."""
+    return (0, 4) if workload in ("d12", "d20", "d26") else (0,)
+
+
+def oracle_sample(idx=(0, 4), workload=WORKLOAD, ns_steps=5):
+    """Time the fp64 oracle on a bounded sample of the workload: one Muon step (ns_steps
+    iterations) of the listed matrices.  Returns (TFLOP/s of algorithmic NS flops, seconds,
+    description, threads, flops)."""
     import numpy as np
     import oracle
     import workloads
@@ -217,14 +240,28 @@ def oracle_sample(idx=(0, 4), workload=WORKLOAD):
     t0 = time.perf_counter()
     for pi, gi, mi, (r, c) in zip(p, g, m, shapes):
         oracle.muon_matrix(pi.numpy(), gi.numpy(), mi.numpy(), lr=np.float32(0.02), beta=np.float32(0.95),
-                           nesterov=True, ns_steps=5)
+                           nesterov=True, ns_steps=ns_steps)
         mm, nn = min(r, c), max(r, c)
-        flops += 5 * (3 * mm * mm * nn + mm ** 3)
+        flops += ns_steps * (3 * mm * mm * nn + mm ** 3)
     dt = time.perf_counter() - t0
-    desc = (f"oracle (fp64 C, OpenMP) full Muon step of {workload} matrices "
+    step = "full Muon step" if ns_steps == 5 else f"Muon step with {ns_steps} Newton-Schulz iteration(s)"
+    desc = (f"oracle (fp64 C, OpenMP) {step} of {workload} matrices "
             + ", ".join(f"{i} ({r}x{c})" for i, (r, c) in zip(idx, shapes))
             + f"; {flops:.3e} algorithmic NS flops")
     return flops / dt / 1e12, dt, desc, oracle.num_threads(), flops
+
+
+def oracle_single_core(workload):
+    """The oracle on one host thread, on a smaller bounded sample (matrix 0, one iteration)."""
+    import oracle
+    oracle.build()
+    n = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        tf, dt, desc, cores, _ = oracle_sample((0,), workload, ns_steps=1)
+    finally:
+        oracle.set_num_threads(n)
+    return {"value": tf, "unit": UNIT, "cores": cores, "sample": f"{desc}; {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -232,12 +269,14 @@ def run_reference(args, rank, world):
         return 0
     import oracle
     oracle.build()
-    # one matrix per step keeps --steps 20 --warmup 3 within a few minutes
+    # the same matrices as the GPU line's cpu_baseline leg; the untimed warm-up steps run the
+    # first of them only, which keeps --steps 20 --warmup 5 within about four minutes
+    sample = default_sample(args.workload)
     for _ in range(args.warmup):
-        oracle_sample((0,), args.workload)
+        oracle_sample(sample[:1], args.workload)
     times, flops_total = [], 0.0
     for _ in range(args.steps):
-        tf, dt, desc, cores, flops = oracle_sample((0,), args.workload)
+        tf, dt, desc, cores, flops = oracle_sample(sample, args.workload)
         times.append(dt)
         flops_total += flops
     value = flops_total / sum(times) / 1e12
@@ -245,7 +284,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": workload_desc(args.workload), "sample": desc},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -267,15 +307,17 @@ def run_ours(args, rank, world, local_rank):
     # CPU oracle timed first (rank 0, N = 1 only), before any GPU work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, dt, desc, cores, _ = oracle_sample((0, 4) if args.workload == WORKLOAD else (0,), args.workload)
+        tf, dt, desc, cores, _ = oracle_sample(default_sample(args.workload), args.workload)
         cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{desc}; {dt:.1f} s"}
+               "sample": f"{desc}; {dt:.1f} s", "cpu_model": cpu_model(),
+               "single_core": oracle_single_core(args.workload)}
 
     wl = args.workload
     shapes = workloads.config_shapes(wl)
     seed = rank  # each replica works on its own stack
     p, g0, m, _ = workloads.make_stack(wl, dev, seed=seed)
-    n_sets = 4
+    # a gradient draw of its own for every step (warm-up and timed), all drawn before timing
+    n_sets = max(1, min(args.warmup + args.steps, MAX_GRAD_SETS))
     grads = [g0] + [[workloads.make_grad(wl, i, s, dev, seed, step) for i, s in enumerate(shapes)]
                     for step in range(1, n_sets)]
     stream = torch.cuda.Stream(device=dev)
@@ -316,7 +358,7 @@ def run_ours(args, rank, world, local_rank):
     mu.muon_get_status(stream)
     step_ms = []
     with ClockSampler(local_rank) as clocks:
-        total_ms = timed(args.steps, step, step_ms)
+        total_ms = timed(args.steps, lambda k: step(args.warmup + k), step_ms)
     mu.muon_get_status(stream)
     # the carried steps one by one (momentum carried, a new gradient set every step)
     step_stats = {k: max_over_ranks(f(step_ms), dist, dev)
@@ -334,7 +376,7 @@ def run_ours(args, rank, world, local_rank):
         step(k)
     mu.muon_get_status(stream)
     mu.muon_kernel_times()
-    timed_ms2 = timed(args.steps, step)
+    timed_ms2 = timed(args.steps, lambda k: step(args.warmup + k))
     kt = mu.muon_kernel_times()
     mu.muon_get_status(stream)
     ns_kinds = ("gram", "poly", "axpy", "axpy_update")
@@ -356,7 +398,8 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
                 "frac_of_burst": ns_tflops / peak_tf, "burst_peak": peak_tf,
                 "traffic": traffic,
-                "traffic_source": "profiles/ns_pair_d26x2_full.md (ncu dram bytes, scaled to d26)",
+                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the d26x2 workload "
+                                   "(2 of the 26 layers) x 13; null once the kernel source has changed"),
                 "avg_launch_ms": ns_ms / max(ns_launches, 1),
                 "alg_flops_per_launch": flops_step * args.steps / max(ns_launches, 1),
                 "executed_over_alg_flops": q["ns_executed_flops"] / q["ns_alg_flops"]}
@@ -381,7 +424,7 @@ def run_ours(args, rank, world, local_rank):
             nm_step(k)
         mu.muon_get_status(stream)
         mu.muon_kernel_times()
-        nm_ms = timed(args.steps, nm_step) / args.steps
+        nm_ms = timed(args.steps, lambda k: nm_step(args.warmup + k)) / args.steps
         nkt = mu.muon_kernel_times()
         mu.muon_get_status(stream)
         normuon = {"ms_per_step": nm_ms, "value": job_tflops(world, flops_step, nm_ms), "unit": UNIT,
@@ -494,10 +537,13 @@ def run_ours(args, rank, world, local_rank):
                 "config": {"workload": workload_desc(wl), "matrices": len(shapes), "elements": elems,
                            "ns_alg_flops_per_step": flops_step,
                            "parallelism": "replicas" if world > 1 else "single-gpu",
-                           "l2": (f"no flush: 4 rotating gradient sets of {4 * elems / 1e9:.2f} GB; weights "
-                                  f"and momentum {4 * elems / 1e9:.2f} GB each"
-                                  + (", all far above the 126 MB L2" if 4 * elems > 126e6 * 4
-                                     else " (below 126 MB L2: small case)")),
+                           "gradients": (f"{n_sets} gradient sets drawn on the device before timing, one per step"
+                                         + ("" if n_sets >= args.warmup + args.steps
+                                            else f" (reused in turn past {n_sets} steps)")),
+                           "l2": (f"no flush: every step reads its own {4 * elems / 1e9:.2f} GB gradient set; "
+                                  f"weights and momentum {4 * elems / 1e9:.2f} GB each"
+                                  + (", all far above the 126 MB L2" if 4 * elems > 126e6
+                                     else " (below the 126 MB L2: small case)")),
                            "state_dtype": "fp32 p/g/m; bf16 Newton-Schulz operands, fp32 accumulation"},
                 "ns_tflops": ns_tflops, "frac_of_bf16_peak": ns_tflops / peak_tf_sus, "frac_of_bf16_burst_peak": ns_tflops / peak_tf,
                 "step_ms": step_stats, "phase_ms_per_step": phase_ms, "timed_ms_with_kernel_events": timed_ms2 / args.steps,
@@ -538,32 +584,43 @@ def run_sweep(args) -> int:
         for _ in range(args.warmup):
             mu.muon_step(sargs, stream=stream)
         mu.muon_get_status(stream)
+        # enough steps for about half a second of timed work, so that the clock sampler (50 ms)
+        # sees the short shapes run too
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mu.muon_step(sargs, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        nsteps = max(args.steps, min(1000, int(500.0 / max(e0.elapsed_time(e1), 1e-3)) + 1))
+        mu.muon_get_status(stream)
         mu.muon_kernel_times()
         times = []
-        for _ in range(args.steps):
-            with torch.cuda.stream(stream):
-                flush.fill_(1)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            mu.muon_step(sargs, stream=stream)
-            e1.record(stream)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1))
+        with ClockSampler(0) as clocks:
+            for _ in range(nsteps):
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                mu.muon_step(sargs, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
         mu.muon_get_status(stream)
         kt = mu.muon_kernel_times()
         info = mu.muon_get_step_info()
         q = mu.muon_plan_query(shapes, workloads.HYPER["ns_steps"])
-        ns_ms = sum(kt[k][0] for k in ("gram", "poly", "axpy", "axpy_update")) / args.steps
-        mom_ms = kt["momentum_norm"][0] / args.steps
+        ns_ms = sum(kt[k][0] for k in ("gram", "poly", "axpy", "axpy_update")) / nsteps
+        mom_ms = kt["momentum_norm"][0] / nsteps
         ms = statistics.median(times)
-        rows.append({"workload": name, "shape": [r, c], "matrices": count, "ms_per_step": ms,
+        rows.append({"workload": name, "shape": [r, c], "matrices": count, "steps": nsteps, "ms_per_step": ms,
                      "ns_tflops": info["ns_alg_flops"] / (ns_ms * 1e-3) / 1e12,
                      "ns_frac_of_sustained_bf16": info["ns_alg_flops"] / (ns_ms * 1e-3) / 1e12 / peak_sus,
                      "executed_over_alg_flops": q["ns_executed_flops"] / q["ns_alg_flops"],
                      "momentum_gbs": 14.0 * count * r * c / (mom_ms * 1e-3) / 1e9,
                      "momentum_frac_of_hbm": 14.0 * count * r * c / (mom_ms * 1e-3) / 1e9 / peak_bw,
-                     "launches_per_step": info["launches"]})
+                     "launches_per_step": info["launches"], "clocks": clocks.summary()})
         mu.muon_destroy()
         del p, g, m, sargs
         torch.cuda.empty_cache()
