@@ -34,10 +34,11 @@
  *    an out-of-range tile) are latched in a device status word and returned by
  *    muon_get_status.
  *  - One process-global context; the functions are not thread-safe.
- *  - The steps of a context share one workspace (and the NorMuon buffers), and
- *    a call orders its work only after earlier work on its own `stream`.  Steps
- *    issued on different streams must therefore be ordered by the caller (an
- *    event, or one stream for all of them); steps that overlap on the GPU race.
+ *  - Steps of a context with the same list of shapes share one workspace (and
+ *    the NorMuon buffers), and every step shares the device status word; a call
+ *    orders its work only after earlier work on its own `stream`.  Steps issued
+ *    on different streams must therefore be ordered by the caller (an event, or
+ *    one stream for all of them); steps that overlap on the GPU race.
  */
 #ifndef MUON_H
 #define MUON_H
@@ -122,10 +123,14 @@ MUON_API muon_status muon_init(const muon_config* cfg);
  *   nesterov 0/1; ns_steps 0..n_coeff_rows (0 gives O = X0).
  * The host arrays are read during the call only.  A matrix must not alias
  * another one of the same call.  Matrices of equal oriented shape are batched
- * into the same launches.  When the list of shapes differs from the previous
- * call's, the workspace is rebuilt; when the weight pointers differ, their
- * tensor maps are re-encoded.  Both synchronise the device (a step still
- * running on another stream may use the old ones).  Otherwise the call
+ * into the same launches.  The context keeps one workspace per distinct list
+ * of shapes, up to 8 (a caller that steps several groups of matrices, such as
+ * the buckets of a sharded step, alternates between them without rebuilding);
+ * a ninth list drops the least recently used workspace, which synchronises
+ * the device.  When the weight pointers differ from the previous call with the
+ * same shapes, their tensor maps are re-encoded, which also synchronises the
+ * device (a step still running on another stream may use the old ones).  The
+ * workspace of a new shape list is allocated by the call.  Otherwise the call
  * only enqueues kernels on `stream` and never blocks the host, so after one
  * uncaptured call with the same shapes and weight pointers a step can be
  * captured into a CUDA graph and replayed, with each step's gradients copied

@@ -25,6 +25,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 constexpr int kKinds = 8;  // momentum, gram, poly, axpy, axpy+update, update, axpy writing O, NorMuon
 constexpr int kMaxCoeffRows = 16;
+constexpr int kMaxPlans = 8;  // workspaces kept, one per distinct shape list (least recently used dropped)
 
 struct ClassPlan {
     int m = 0, n = 0, transposed = 0;
@@ -92,7 +93,8 @@ struct Context {
     unsigned long long timeout_ns = 5000000000ull;
     EncodeTiledFn encode = nullptr;
     unsigned int* status = nullptr;
-    Plan* plan = nullptr;
+    std::vector<Plan*> plans;       // most recently used first
+    Plan* last = nullptr;           // the plan of the last step (debug copies)
     muon_step_info info{};
     std::vector<cudaEvent_t> event_pool;
     std::vector<PendingTime> pending;
@@ -522,7 +524,7 @@ const char* muon_status_string(muon_status s) {
 muon_status muon_destroy(void) {
     if (!g_ctx) return MUON_OK;
     cudaDeviceSynchronize();
-    free_plan(g_ctx->plan);
+    for (Plan* P : g_ctx->plans) free_plan(P);
     for (auto& pt : g_ctx->pending) {
         cudaEventDestroy(pt.a);
         cudaEventDestroy(pt.b);
@@ -622,19 +624,29 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
-    if (!same_shapes(ctx->plan, shapes, n_mats)) {
-        if (ctx->plan) {
-            // work of earlier steps, on any stream, may still use the old workspace
-            if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
-            free_plan(ctx->plan);
-            ctx->plan = nullptr;
+    // the plan of this shape list: reused when cached (moved to the front), else built, dropping
+    // the least recently used one when kMaxPlans are held
+    Plan* P = nullptr;
+    for (size_t k = 0; k < ctx->plans.size(); ++k) {
+        if (same_shapes(ctx->plans[k], shapes, n_mats)) {
+            P = ctx->plans[k];
+            ctx->plans.erase(ctx->plans.begin() + static_cast<long>(k));
+            break;
         }
-        Plan* P = nullptr;
+    }
+    if (!P) {
+        if (static_cast<int>(ctx->plans.size()) >= kMaxPlans) {
+            // work of earlier steps, on any stream, may still use the dropped workspace
+            if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
+            if (ctx->last == ctx->plans.back()) ctx->last = nullptr;
+            free_plan(ctx->plans.back());
+            ctx->plans.pop_back();
+        }
         const muon_status st = build_plan(ctx, shapes, n_mats, &P);
         if (st != MUON_OK) return st;
-        ctx->plan = P;
     }
-    Plan* P = ctx->plan;
+    ctx->plans.insert(ctx->plans.begin(), P);
+    ctx->last = P;
     if (nm) {
         const muon_status st = ensure_normuon(ctx, P);
         if (st != MUON_OK) return st;
@@ -967,8 +979,8 @@ muon_status muon_kernel_times(double* ms_out, int* launches_out, int n_kinds) {
 muon_status muon_debug_copy_ns_output(int mat, float* dst_device, muon_stream_t stream) {
     Context* ctx = g_ctx;
     if (!ctx) return MUON_ERR_NOT_INITIALIZED;
-    if (!(ctx->debug & MUON_DEBUG_KEEP_O) || !ctx->plan || !dst_device) return MUON_ERR_INVALID_ARG;
-    Plan* P = ctx->plan;
+    if (!(ctx->debug & MUON_DEBUG_KEEP_O) || !ctx->last || !dst_device) return MUON_ERR_INVALID_ARG;
+    Plan* P = ctx->last;
     if (mat < 0 || mat >= static_cast<int>(P->shapes.size())) return MUON_ERR_INVALID_ARG;
     const size_t bytes = static_cast<size_t>(P->shapes[mat].rows) * P->shapes[mat].cols * sizeof(float);
     return cudaMemcpyAsync(dst_device, P->dbg_O[mat], bytes, cudaMemcpyDeviceToDevice,
@@ -980,9 +992,9 @@ muon_status muon_debug_copy_ns_output(int mat, float* dst_device, muon_stream_t 
 muon_status muon_debug_copy_norms(float* dst_host, int n) {
     Context* ctx = g_ctx;
     if (!ctx) return MUON_ERR_NOT_INITIALIZED;
-    if (!ctx->plan || !dst_host || n < 0 || n > static_cast<int>(ctx->plan->shapes.size()))
+    if (!ctx->last || !dst_host || n < 0 || n > static_cast<int>(ctx->last->shapes.size()))
         return MUON_ERR_INVALID_ARG;
-    Plan* P = ctx->plan;
+    Plan* P = ctx->last;
     std::vector<float> tmp(P->shapes.size());
     if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
     if (cudaMemcpy(tmp.data(), P->norms, tmp.size() * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)

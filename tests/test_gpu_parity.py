@@ -317,3 +317,16 @@ def test_debug_copy_of_o_matches_the_oracle_and_leaves_the_step_unchanged(case):
     run_and_check(p, g, m, keep_o=True, tol_o=tol)
     for a, b in zip(plain, p + m):
         assert torch.equal(a, b)
+
+
+def test_several_shape_lists_keep_their_workspaces():
+    # the context keeps a workspace per shape list (up to 8): alternating lists must give the
+    # oracle's result every time, and a ninth list (dropping the least recently used) too
+    lists = [[(64, 64), (128, 64)], [(64, 128)], [(96, 96), (64, 64)], [(128, 128)], [(64, 192)], [(192, 64)],
+             [(160, 160)], [(72, 72)], [(64, 64), (64, 64), (128, 128)]]
+    # lists 0..7 fill the cache; list 8 then drops the least recently used, list 2; 0 is still held,
+    # 2 is rebuilt
+    order = [0, 1, 2, 0, 1, 3, 4, 5, 6, 7, 8, 0, 2]
+    for step, k in enumerate(order):
+        p, g, m, _ = workloads.make_custom(lists[k], "cuda", tag=f"plans{step}")
+        run_and_check(p, g, m, ns_steps=3)

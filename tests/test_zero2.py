@@ -68,43 +68,76 @@ def _rank_grads(rank, step):
     return [workloads.make_grad("zero2", 100 * rank + i, s, "cpu", 0, step) for i, s in enumerate(SHAPES)]
 
 
-def _worker(rank, world, port, out):
+def _worker(rank, world, port, buckets, zero_copy, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         params = [workloads.make_param("zero2", i, s, "cpu", 0) for i, s in enumerate(SHAPES)]
-        sharded = mu.zero2.ShardedMuon(params, compute=oracle_compute)
+        ids = [id(p) for p in params]
+        sharded = mu.zero2.ShardedMuon(params, compute=oracle_compute, buckets=buckets)
+        # the caller's tensors are the same objects, now living in the bucket buffers
+        assert [id(p) for p in params] == ids
+        assert all(torch.equal(p, workloads.make_param("zero2", i, s, "cpu", 0))
+                   for i, (p, s) in enumerate(zip(params, SHAPES)))
         for step in range(2):
-            sharded.step(_rank_grads(rank, step), **HYPER)
+            if zero_copy:
+                for i, g in enumerate(_rank_grads(rank, step)):
+                    sharded.grad_view(i).copy_(g)
+                sharded.step(**HYPER)
+            else:
+                sharded.step(_rank_grads(rank, step), **HYPER)
         out[rank] = ([p.numpy().copy() for p in params], sharded.owner,
-                     {i: m.numpy().copy() for i, m in sharded.momentum.items()})
+                     {i: m.numpy().copy() for i, m in sharded.momentum.items()}, len(sharded.buckets))
     finally:
         dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_match_one_process_on_the_mean_gradient():
-    world = 2
+@pytest.mark.parametrize("world,buckets,zero_copy", [(2, 1, False), (2, 2, False), (3, 3, True), (3, 2, False)])
+def test_gloo_ranks_match_one_process_on_the_mean_gradient(world, buckets, zero_copy):
     with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
-        mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+        mp.spawn(_worker, args=(world, _free_port(), buckets, zero_copy, out), nprocs=world, join=True)
         res = dict(out)
+    assert res[0][3] == buckets
     # every rank ends with the same weights
-    for a, b in zip(res[0][0], res[1][0]):
-        assert np.array_equal(a, b)
+    for r in range(1, world):
+        for a, b in zip(res[0][0], res[r][0]):
+            assert np.array_equal(a, b)
     owner = res[0][1]
-    assert sorted(set(owner)) == [0, 1]
-    # reference: one process, the mean of the ranks' gradients, full momentum
+    assert sorted(set(owner)) == list(range(world))
+    # reference: one process, the mean of the ranks' gradients, full momentum (the oracle)
     params = [workloads.make_param("zero2", i, s, "cpu", 0).numpy() for i, s in enumerate(SHAPES)]
     moms = [np.zeros(s, np.float32) for s in SHAPES]
     for step in range(2):
-        g = [(a + b) * np.float32(0.5) for a, b in zip((t.numpy() for t in _rank_grads(0, step)),
-                                                       (t.numpy() for t in _rank_grads(1, step)))]
+        per_rank = [[t.numpy() for t in _rank_grads(r, step)] for r in range(world)]
+        g = [(sum(gs[i].astype(np.float64) for gs in per_rank) / world).astype(np.float32) for i in range(len(SHAPES))]
         for i in range(len(SHAPES)):
             params[i], moms[i], _ = oracle.muon_matrix(params[i], g[i], moms[i], lr=np.float32(0.02),
                                                        beta=np.float32(0.95), nesterov=True, ns_steps=3)
     for i in range(len(SHAPES)):
         assert np.allclose(res[0][0][i], params[i], rtol=0, atol=1e-6), i
         assert np.allclose(res[owner[i]][2][i], moms[i], rtol=0, atol=1e-9), i
+
+
+def test_buckets_cut_at_about_equal_sizes():
+    # host logic of the split, through a one-rank gloo group: consecutive matrices in index
+    # order, every matrix in exactly one bucket, at most the requested count, sizes within one
+    # matrix of the mean
+    params = [torch.zeros(s) for s in workloads.config_shapes("d2")]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        for nb in (1, 2, 3, 12, 20):
+            sh = mu.zero2.ShardedMuon([p.clone() for p in params], compute=oracle_compute, buckets=nb)
+            idx = [i for bk in sh.buckets for i in bk.index]
+            assert idx == list(range(len(params)))
+            assert 1 <= len(sh.buckets) <= min(nb, len(params)) and all(bk.index for bk in sh.buckets)
+            if nb <= 3:
+                assert len(sh.buckets) == nb
+            sizes = [sum(params[i].numel() for i in bk.index) for bk in sh.buckets]
+            assert max(sizes) <= sum(sizes) / len(sizes) + max(p.numel() for p in params)
+    finally:
+        dist.destroy_process_group()
 
 
 def _failing_worker(rank, world, port, case, out):
@@ -120,7 +153,7 @@ def _failing_worker(rank, world, port, case, out):
             raise RuntimeError("update failed on this rank")
 
         compute = broken_compute if (case == "raises" and rank == 1) else oracle_compute
-        sharded = mu.zero2.ShardedMuon(params, compute=compute)
+        sharded = mu.zero2.ShardedMuon(params, compute=compute, buckets=2)
         if case == "never_joins" and rank == 1:
             time.sleep(6.0)  # holds the group open past the survivor's timeout, then leaves
             out[rank] = ("left", None, None)
