@@ -160,9 +160,10 @@ MUON_API muon_status muon_step(float* const params[], const float* const grads[]
  *                      aligned, caller-owned, updated in place (zero-initialise
  *                      it before the first step)
  *   beta2 in [0, 1), eps2 >= 0; ns_steps >= 1; other arguments as muon_step.
- * O is materialised in an fp32 workspace (one more allocation of the size of
- * the weights, made by the first call on a shape list); the per-row reduction
- * is deterministic.  With MUON_DEBUG_KEEP_O, muon_debug_copy_ns_output
+ * O is materialised in a bf16 workspace (one more allocation of half the size
+ * of the weights, made by the first call on a shape list), and the row
+ * statistics and the update read it from there; the per-row reduction is
+ * deterministic.  With MUON_DEBUG_KEEP_O, muon_debug_copy_ns_output
  * returns the scaled update step_i ratio O.  Errors as muon_step.
  */
 MUON_API muon_status muon_step_normuon(float* const params[], const float* const grads[],

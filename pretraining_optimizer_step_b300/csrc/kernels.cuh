@@ -74,7 +74,7 @@ enum GemmMode : int {
     MODE_POLY = 1,        // B' = b A + c A A + a I
     MODE_AXPY = 2,        // X' = s B' X
     MODE_AXPY_FINAL = 3,  // O = s B' X; p -= scale O
-    MODE_AXPY_O = 4,      // O = s B' X written in fp32 (stored layout) for the NorMuon pass
+    MODE_AXPY_O = 4,      // O = s B' X written in bf16 (stored layout) for the NorMuon pass
 };
 
 // ------------------------------------------------------------------ NorMuon scaling
@@ -85,7 +85,7 @@ constexpr int kNormWarps = 8;                // 256 threads
 constexpr int kNormRowsPerWarp = 4;
 constexpr int kNormRowsPerCta = kNormWarps * kNormRowsPerWarp;
 struct NormuonMat {
-    const float* O;       // stored rows x cols (workspace)
+    const __nv_bfloat16* O;  // stored rows x cols, bf16 (workspace)
     float* V;             // caller-owned second moments, rows floats
     float* p;             // weights
     float* dbg;           // O' (stored layout) when the debug copy is kept, else nullptr
@@ -163,7 +163,8 @@ struct PairParams {
     float lr;
     const CUtensorMap* p_maps;    // per step position: fp32 weights (stored layout), box 32 x 32, 128B swizzle
     const CUtensorMap* dbg_maps;  // per step position (O, stored layout) or nullptr
-    const CUtensorMap* o_maps;    // MODE_AXPY_O: per step position, the fp32 O buffer (stored layout)
+    const CUtensorMap* o_maps;    // MODE_AXPY_O: per step position, the bf16 O buffer (stored layout), box 32 x 32,
+                                  // 64B swizzle
     unsigned int* status;
     unsigned long long timeout_ns;
     int inject_lost_load;

@@ -64,7 +64,7 @@ struct Plan {
     std::vector<float*> mapped_p;   // params the device p_maps describe, by step index
     // NorMuon resources (allocated by the first muon_step_normuon on this plan)
     char* nm_arena = nullptr;
-    std::vector<float*> o_bufs;     // fp32 O per matrix (stored layout), by step index
+    std::vector<__nv_bfloat16*> o_bufs;  // bf16 O per matrix (stored layout), by step index
     CUtensorMap* o_maps = nullptr;  // device, by position
     float* nm_step = nullptr;       // step_i of every stored row, matrices at row_base
     int* nm_row_base = nullptr;     // device, by position
@@ -371,7 +371,7 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
     return MUON_OK;
 }
 
-// Workspace of the NorMuon pass: fp32 O per matrix, their tensor maps, the per-row
+// Workspace of the NorMuon pass: bf16 O per matrix, their tensor maps, the per-row
 // step sizes and the per-matrix reduction state.  Built once per plan.
 muon_status ensure_normuon(Context* ctx, Plan* P) {
     if (P->nm_arena) return MUON_OK;
@@ -391,7 +391,7 @@ muon_status ensure_normuon(Context* ctx, Plan* P) {
     }
     for (int i = 0; i < n; ++i) {
         off_o[i] = off;
-        off = align_up(off + static_cast<size_t>(P->shapes[i].rows) * P->shapes[i].cols * sizeof(float), 1024);
+        off = align_up(off + static_cast<size_t>(P->shapes[i].rows) * P->shapes[i].cols * sizeof(__nv_bfloat16), 1024);
     }
     const size_t off_maps = off; off = align_up(off + n * sizeof(CUtensorMap), 256);
     const size_t off_step = off; off = align_up(off + static_cast<size_t>(total_rows) * sizeof(float), 256);
@@ -405,7 +405,7 @@ muon_status ensure_normuon(Context* ctx, Plan* P) {
         return MUON_ERR_OUT_OF_MEMORY;
     }
     P->o_bufs.resize(n);
-    for (int i = 0; i < n; ++i) P->o_bufs[i] = reinterpret_cast<float*>(a + off_o[i]);
+    for (int i = 0; i < n; ++i) P->o_bufs[i] = reinterpret_cast<__nv_bfloat16*>(a + off_o[i]);
     P->o_maps = reinterpret_cast<CUtensorMap*>(a + off_maps);
     P->nm_step = reinterpret_cast<float*>(a + off_step);
     P->nm_row_base = reinterpret_cast<int*>(a + off_rb);
@@ -415,7 +415,8 @@ muon_status ensure_normuon(Context* ctx, Plan* P) {
     std::vector<CUtensorMap> om(n);
     for (int k = 0; k < n; ++k) {
         const int i = P->order[k];
-        if (encode_f32_map(ctx->encode, &om[k], P->o_bufs[i], P->shapes[i].rows, P->shapes[i].cols) != MUON_OK) {
+        if (encode_map_ex(ctx->encode, &om[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P->o_bufs[i], P->shapes[i].cols,
+                          P->shapes[i].rows, 0, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) != MUON_OK) {
             cudaFree(a);
             return MUON_ERR_CUDA;
         }

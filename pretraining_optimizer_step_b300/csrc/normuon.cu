@@ -11,8 +11,9 @@
 //   ratio = sqrt(sum_i v_mean_i) / max(sqrt(sum_i v_mean_i step_i^2), 1e-10)
 //   p_ij <- p_ij - lr sqrt(max(1, r/c)) step_i ratio O_ij       (keeps ||O||_F)
 //
+// O arrives in bf16 (stored layout), written by the last Newton-Schulz launch.
 // normuon_rows_kernel: one warp per stored row (4 rows per warp, 32 per CTA) reads the row
-//   of O (fp32, 16-byte loads), reduces its squares in a fixed order, updates V
+//   of O (16-byte loads of 8 bf16), reduces its squares in fp32 in a fixed order, updates V
 //   and writes step_i; the last CTA of a matrix (atomic ticket) adds the CTAs'
 //   double partial sums, spread over its threads in a fixed order, and
 //   publishes ratio.  Deterministic.
@@ -35,6 +36,20 @@ __device__ __forceinline__ int find_normuon_mat(const NormuonParams& P, int x, b
     return lo;
 }
 
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// sum of squares of the 8 bf16 values of a 16-byte word, added to acc
+__device__ __forceinline__ float sq8(uint4 w, float acc) {
+    acc = fmaf(bf_lo(w.x), bf_lo(w.x), acc);
+    acc = fmaf(bf_hi(w.x), bf_hi(w.x), acc);
+    acc = fmaf(bf_lo(w.y), bf_lo(w.y), acc);
+    acc = fmaf(bf_hi(w.y), bf_hi(w.y), acc);
+    acc = fmaf(bf_lo(w.z), bf_lo(w.z), acc);
+    acc = fmaf(bf_hi(w.z), bf_hi(w.z), acc);
+    acc = fmaf(bf_lo(w.w), bf_lo(w.w), acc);
+    return fmaf(bf_hi(w.w), bf_hi(w.w), acc);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant__ NormuonParams P) {
@@ -47,23 +62,20 @@ __global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant
     for (int rw = 0; rw < kNormRowsPerWarp; ++rw) {
         const int row = (cta - M.cta_begin) * kNormRowsPerCta + rw * kNormWarps + warp;
         if (row >= M.rows) break;
-        const float4* o4 = reinterpret_cast<const float4*>(M.O + static_cast<size_t>(row) * M.cols);
+        const uint4* o8 = reinterpret_cast<const uint4*>(M.O + static_cast<size_t>(row) * M.cols);
         // four independent sums, so four loads per lane are in flight
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        const int nq = M.cols >> 2;
+        const int nq = M.cols >> 3;
         int q = lane;
         for (; q + 96 < nq; q += 128) {
-            const float4 o0 = __ldcg(o4 + q), o1 = __ldcg(o4 + q + 32);
-            const float4 o2 = __ldcg(o4 + q + 64), o3 = __ldcg(o4 + q + 96);
-            a0 = fmaf(o0.w, o0.w, fmaf(o0.z, o0.z, fmaf(o0.y, o0.y, fmaf(o0.x, o0.x, a0))));
-            a1 = fmaf(o1.w, o1.w, fmaf(o1.z, o1.z, fmaf(o1.y, o1.y, fmaf(o1.x, o1.x, a1))));
-            a2 = fmaf(o2.w, o2.w, fmaf(o2.z, o2.z, fmaf(o2.y, o2.y, fmaf(o2.x, o2.x, a2))));
-            a3 = fmaf(o3.w, o3.w, fmaf(o3.z, o3.z, fmaf(o3.y, o3.y, fmaf(o3.x, o3.x, a3))));
+            const uint4 o0 = __ldcg(o8 + q), o1 = __ldcg(o8 + q + 32);
+            const uint4 o2 = __ldcg(o8 + q + 64), o3 = __ldcg(o8 + q + 96);
+            a0 = sq8(o0, a0);
+            a1 = sq8(o1, a1);
+            a2 = sq8(o2, a2);
+            a3 = sq8(o3, a3);
         }
-        for (; q < nq; q += 32) {
-            const float4 o = __ldcg(o4 + q);
-            a0 = fmaf(o.w, o.w, fmaf(o.z, o.z, fmaf(o.y, o.y, fmaf(o.x, o.x, a0))));
-        }
+        for (; q < nq; q += 32) a0 = sq8(__ldcg(o8 + q), a0);
         float acc = (a0 + a1) + (a2 + a3);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -144,7 +156,8 @@ __global__ void __launch_bounds__(256) normuon_update_kernel(const __grid_consta
         if (row >= M.rows || col >= M.cols) continue;
         const size_t off = static_cast<size_t>(row) * M.cols + col;
         const float sr = step[row] * ratio;
-        const float4 o = __ldcs(reinterpret_cast<const float4*>(M.O + off));
+        const uint2 ob = __ldcs(reinterpret_cast<const uint2*>(M.O + off));
+        const float4 o = make_float4(bf_lo(ob.x), bf_hi(ob.x), bf_lo(ob.y), bf_hi(ob.y));
         float4 w = *reinterpret_cast<float4*>(M.p + off);
         const float sc = lr_aspect * sr;
         w.x = fmaf(-sc, o.x, w.x);

@@ -8,7 +8,7 @@
 //   MODE_POLY        B' = b A + c A A + a I      A symmetric: A A = A A^T, same operand both sides
 //   MODE_AXPY        X' = s B' X                 X read MN-major as the B operand
 //   MODE_AXPY_FINAL  O = s B' X in fp32, p += -lr sqrt(max(1, r/c)) O (TMA reduce-add)
-//   MODE_AXPY_O      O = s B' X in fp32, stored (stored layout) for the NorMuon pass
+//   MODE_AXPY_O      O = s B' X, stored in bf16 (stored layout) for the NorMuon pass
 // Folding a I into the polynomial makes a X + B X = (B + a I) X a plain product, so the
 // axpy epilogues read nothing but the accumulator; the only numerical change is one bf16
 // rounding of B's diagonal entries plus a.  The final launch never reads the weights: it
@@ -106,6 +106,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Byte offsets inside the swizzled 32 x 32 subtiles the epilogue TMA maps use.
 // bf16, 64-byte rows, 64B swizzle: 16-byte unit u of row r lives at unit u ^ ((r >> 1) & 3).
 __device__ __forceinline__ uint32_t sw64_unit(int r, int u) { return r * 64 + ((u ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_unit(r, c >> 3) + ((c & 7) << 1); }
 // fp32, 128-byte rows, 128B swizzle: 16-byte unit u of row r lives at unit u ^ (r & 7).
 __device__ __forceinline__ uint32_t sw128_unit(int r, int u) { return r * 128 + ((u ^ (r & 7)) << 4); }
 __device__ __forceinline__ uint32_t sw128_elem(int r, int c) { return sw128_unit(r, c >> 2) + ((c & 3) << 2); }
@@ -317,10 +318,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         //   final, debug copy of O (24 KiB): 2 output slot pairs {weight change, O} of 8 KiB
         //   gram  (8 KiB):   4 output slots of bf16
         //   poly  (8 KiB):   2 bf16 input slots (A) + 2 output slots of bf16
-        //   axpy  (8 KiB):   4 output slots of bf16
-        //   axpy_o (8 KiB):  2 output slots of fp32 O
+        //   axpy, axpy_o (8 KiB): 4 output slots of bf16 (axpy_o: O in the stored layout)
         const bool o_mode = P.mode == MODE_AXPY_O;
-        const bool f32_out = final_mode || o_mode;
+        const bool f32_out = final_mode;
         const int n_in = has_in ? 2 : 0;
         const int in_stride = 2048;
         const int n_out = (f32_out || P.mode == MODE_POLY) ? 2 : 4;
@@ -465,18 +465,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                     *reinterpret_cast<float*>(o_slot + sw128_elem(j, lane)) = v[j];
                             }
                         }
-                    } else if (o_mode) {
-                        // fp32 O subtile in the stored layout (rows = stored rows)
-                        if (!transposed) {
+                    } else if (o_mode && transposed) {
+                        // bf16 O subtile in the stored layout: stored rows are oriented columns j,
+                        // stored columns are lanes (one 64-byte row per j, 2 bytes per lane)
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                *reinterpret_cast<float4*>(out_slot + sw128_unit(lane, u)) =
-                                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                *reinterpret_cast<float*>(out_slot + sw128_elem(j, lane)) = v[j];
-                        }
+                        for (int j = 0; j < 32; ++j)
+                            *reinterpret_cast<__nv_bfloat16*>(out_slot + sw64_elem(j, lane)) = __float2bfloat16_rn(v[j]);
                     } else {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {

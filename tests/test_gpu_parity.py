@@ -79,6 +79,12 @@ def small_side_tol(shape):
     return TOL_O if min(shape) >= 64 else 6e-2
 
 
+def pe_small_side_tol(shape):
+    # with the Polar Express table, sides below 64 reach 8e-2 to 9e-2 in the rounding model (the
+    # rows' large a I and b A terms cancel on bf16 operands); tests/test_rounding_model.py
+    return TOL_O if min(shape) >= 64 else 1.2e-1
+
+
 @pytest.mark.parametrize("ns_steps,tol", [(1, 5e-3), (5, small_side_tol)])
 def test_ragged_and_edge_shapes(ns_steps, tol):
     # one iteration is checked tightly (bf16 rounding of X0 gives about 1.7e-3),
@@ -111,7 +117,7 @@ def test_pages_polar_express_rows():
 def test_derived_polar_express_table(case):
     # the full five-row table of the Polar Express construction (the two rows the pages print
     # and the three derived ones; tests/test_polar_express.py pins it on the CPU).  A model of
-    # the kernels' rounding gives O errors of 1.3e-2 to 1.7e-2 with it on the d2 shapes
+    # the kernels' rounding gives O errors of 1.3e-2 to 1.4e-2 with it on sides of 64 and more
     rows = [tuple(r) for r in mu.POLAR_EXPRESS_COEFFS]
     mu.muon_destroy()
     mu.muon_init(coeffs=rows, wait_timeout_s=2.0)
@@ -119,7 +125,7 @@ def test_derived_polar_express_table(case):
         p, g, m, _ = workloads.make_stack("d2", "cuda")
     else:
         p, g, m, _ = workloads.make_custom(RAGGED, "cuda", tag="ragged")
-    run_and_check(p, g, m, coeffs=np.array(rows), ns_steps=5, tol_o=small_side_tol)
+    run_and_check(p, g, m, coeffs=np.array(rows), ns_steps=5, tol_o=pe_small_side_tol)
 
 
 def test_per_iteration_rows_switch():
