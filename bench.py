@@ -173,9 +173,11 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) per Newton-Schulz launch at d26, from one ncu capture of the
-# d26x2 workload (the same shapes, 2 of the 26 layers) scaled by 13, and the sha256 of the
-# kernel source it was taken on.  The figure is reported only while the source is unchanged.
-NS_PAIR_TRAFFIC = {"bytes_per_launch_d26": None, "source_sha256": None}
+# d26x2 workload (the same shapes, 2 of the 26 layers): one axpy, Gram, polynomial and final
+# launch, averaged with a step's launch counts (4, 5, 5, 1) and scaled by 13; and the sha256
+# of the kernel source it was taken on.  The figure is reported only while the source is
+# unchanged.
+NS_PAIR_TRAFFIC = {"bytes_per_launch_d26": 2.3745e+09, "source_sha256": "867309879dc16fecdc3ac2ad7e079f92accf0cd291d101e9a0a3a2bbc5c42535"}
 
 
 def ns_pair_traffic():
@@ -517,7 +519,40 @@ def run_ours(args, rank, world, local_rank):
             ev1.synchronize()
             return ev0.elapsed_time(ev1)
 
+        def link_gbs():
+            """The host link alone: one step's gradient upload, one weight download, and both
+            overlapped (pinned buffers, the copy streams the end-to-end steps use)."""
+            out = {}
+            for name, ups, downs in (("h2d", True, False), ("d2h", False, True), ("both", True, True)):
+                barrier()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                copy_in.wait_event(e0)
+                copy_out.wait_event(e0)
+                done = []
+                if ups:
+                    with torch.cuda.stream(copy_in):
+                        for d, h in zip(dev_g[0], host_g[0]):
+                            d.copy_(h, non_blocking=True)
+                        done.append(torch.cuda.Event())
+                        done[-1].record(copy_in)
+                if downs:
+                    with torch.cuda.stream(copy_out):
+                        for h, s_ in zip(host_p, snap):
+                            h.copy_(s_, non_blocking=True)
+                        done.append(torch.cuda.Event())
+                        done[-1].record(copy_out)
+                for ev in done:
+                    stream.wait_event(ev)
+                e1.record(stream)
+                e1.synchronize()
+                nbytes = (h2d if ups else 0) + (d2h if downs else 0)
+                out[name] = nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+            return out
+
         e2e_steps = max(2, min(args.steps, 8))
+        link_gbs()                                  # warm-up of the copy paths
+        link = link_gbs()
         e2e_run(2)                                  # warm-up of the copy path
         barrier()
         ms_e2e = max_over_ranks(e2e_run(e2e_steps), dist, dev) / e2e_steps
@@ -525,6 +560,8 @@ def run_ours(args, rank, world, local_rank):
         mu.muon_get_status(stream)
         e2e = {"value": job_tflops(world, flops_step, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "link_gbs": link,
+               "link_bound_ms_per_step": (h2d + d2h) / (link["both"] * 1e9) * 1e3,
                "path": ("pinned host grads -> muon_step (C ABI) -> pinned host params; uploads double-buffered "
                         "on one copy stream, weights snapshotted on the device and downloaded on another, "
                         "overlapping the next step")}

@@ -731,6 +731,10 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
             P->mapped_p.assign(params, params + n_mats);
         }
         static PairParams pp;  // ~5 KiB: kept off the stack
+        // step position of every class's first matrix (positions are class-ordered)
+        std::vector<int> class_base(nclass, 0);
+        for (int c = 1; c < nclass; ++c)
+            class_base[c] = class_base[c - 1] + static_cast<int>(P->classes[c - 1].mats.size());
         for (int it = 0; it < ns_steps; ++it) {
             const double* row = &ctx->coeffs[3 * it];
             const int pin = it & 1, pout = pin ^ 1;
@@ -760,11 +764,17 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                                               ? 1
                                               : 0;
                     if (pp.inject_lost_load) ctx->injected = true;
+                    // The clusters take tiles round-robin in launch order, so the classes whose tiles
+                    // run longest (deepest K) go first and the last wave is made of the shortest
+                    // tiles; within a class the tiles of one matrix stay adjacent (their operands
+                    // share L2).
+                    int ord[kMaxClasses];
+                    for (int k = 0; k < gc; ++k) ord[k] = g0 + k;
+                    auto depth = [&](int c) { return mode == MODE_GRAM ? P->classes[c].n : P->classes[c].m; };
+                    std::stable_sort(ord, ord + gc, [&](int x, int y) { return depth(x) > depth(y); });
                     int tiles = 0;
-                    int mat_base = 0;
-                    for (int k = 0; k < g0; ++k) mat_base += static_cast<int>(P->classes[k].mats.size());
                     for (int k = 0; k < gc; ++k) {
-                        const ClassPlan& cp = P->classes[g0 + k];
+                        const ClassPlan& cp = P->classes[ord[k]];
                         PairClass& C = pp.cls[k];
                         const int G = static_cast<int>(cp.mats.size());
                         C.m = cp.m;
@@ -773,7 +783,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                         C.tile_begin = tiles;
                         C.row_blocks = cp.row_blocks;
                         C.transposed = cp.transposed;
-                        C.mat_base = mat_base;
+                        C.mat_base = class_base[ord[k]];
                         if (mode == MODE_GRAM) {
                             C.tiles_per_mat = cp.sym_pair_tiles;
                             C.col_groups = cp.col_pairs;
@@ -800,7 +810,6 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                             pp.tmOut[k] = cp.epiX[pout];
                         }
                         tiles += C.tiles_per_mat * G;
-                        mat_base += G;
                     }
                     pp.total_tiles = tiles;
                     const int clusters = std::min(tiles, ctx->max_clusters);
