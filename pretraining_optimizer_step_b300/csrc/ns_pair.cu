@@ -198,7 +198,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const bool a_symm = P.mode != MODE_GRAM;    // poly: A; axpy: B'
             const int a_first = pt.rb - rank;           // the pair's first row block
             const int b_first = pt.c0 >> 7;             // the pair's first column block (poly)
-            const uint32_t total_bytes = 2u * (2u * kPairPanelBytes + static_cast<uint32_t>(half) * kPairBK * 2u);
+            // a diagonal tile of a symmetric product with N = 256: each CTA's half of the B operand is
+            // its own A panel (same rows, K block and orientation), so only the A panels are loaded
+            const bool diag = sym && pt.ncols == 256 && b_first == a_first;
+            const uint32_t total_bytes =
+                diag ? 2u * 2u * kPairPanelBytes
+                     : 2u * (2u * kPairPanelBytes + static_cast<uint32_t>(half) * kPairBK * 2u);
             for (int kb = 0; kb < C.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, P.timeout_ns)) {
                     latch_status(P.status, STATUS_TIMEOUT);
@@ -222,7 +227,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, k0 + 64 * h, pt.rb * 128, pt.mat);
                     }
                 }
-                if (sym) {
+                if (diag) {
+                    // the B halves are the A panels just loaded
+                } else if (sym) {
                     const bool b_tr = P.mode == MODE_POLY && kb <= b_first;
                     if (b_tr) {
                         // MN-major B half: one 64 x 128 panel per 64 of this CTA's N rows
@@ -259,6 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const bool a_symm = P.mode != MODE_GRAM;
             const int a_first = pt.rb;            // rank 0's row block = the pair's first
             const int b_first = pt.c0 >> 7;
+            const bool diag = sym && pt.ncols == 256 && b_first == a_first;  // B halves = A panels
             if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_flag, P.timeout_ns)) {
                 latch_status(P.status, STATUS_TIMEOUT);
                 abort_flag = 1;
@@ -275,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t sa = tiles_base + stage * kPairStageBytes;
-                const uint32_t sb = sa + 2 * kPairPanelBytes;
+                const uint32_t sb = diag ? sa : sa + 2 * kPairPanelBytes;
                 const int a_mn = (a_symm && kb <= a_first) ? 1 : 0;
                 const int b_mn = sym ? ((P.mode == MODE_POLY && kb <= b_first) ? 1 : 0) : 1;
                 const uint32_t idesc = idesc_bf16_f32_ab(256, pt.ncols, a_mn, b_mn);
