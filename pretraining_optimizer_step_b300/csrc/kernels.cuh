@@ -120,7 +120,8 @@ cudaError_t launch_update(const UpdateParams& p, cudaStream_t s);
 // A cluster of two CTAs computes a 256 x N tile (N = 256, or 128 for a ragged
 // last column tile) with tcgen05.mma.cta_group::2: each CTA holds 128 rows of
 // the A operand and N/2 rows of the B operand per pipeline stage, and receives
-// its 128 rows of the accumulator in its own TMEM.
+// its 128 rows of the accumulator in its own TMEM.  A row pair whose second
+// block does not exist runs as a 128 x N tile (M = 128: 64 rows per CTA).
 // Each pipeline stage covers 128 of K (8 MMAs of K 16): per CTA two 16 KiB
 // panels of A (128 rows x 64 K, 128B-swizzled) and two of its B half.  Fewer,
 // deeper stages amortise the per-stage barrier round trip of the MMA issuer.
@@ -152,6 +153,7 @@ struct PairParams {
                                      // use tmA); axpy MN-major box 64 cols x 128 K
     CUtensorMap tmIn[kMaxClasses];   // epilogue input (poly: A, axpy: X), bf16 box 32 x 32, 64B swizzle
     CUtensorMap tmOut[kMaxClasses];  // epilogue output (gram: A, poly: B, axpy: X'), bf16 box 32 x 32, 64B swizzle
+    CUtensorMap tmA64[kMaxClasses];  // A side of a half tile (M = 128): K-major box 64 (K) x 64 rows
     PairClass cls[kMaxClasses];
     int nclasses;
     int total_tiles;      // pair tiles

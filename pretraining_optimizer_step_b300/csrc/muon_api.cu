@@ -36,7 +36,7 @@ struct ClassPlan {
     // A-side K-major maps (box 64 x 128), B-side K-major maps (box 64 x 64), the MN-major X map
     // of the axpy B operand (box 64 x 128), and epilogue subtile maps (bf16 32 x 32)
     CUtensorMap tmXk[2], tmAk, tmBk;
-    CUtensorMap tmXk64[2], tmAk64, tmXmn128[2], epiX[2], epiA, epiB;
+    CUtensorMap tmXk64[2], tmAk64, tmBk64, tmXmn128[2], epiX[2], epiA, epiB;
     int row_blocks = 0, col_tiles = 0;
     int col_pairs = 0, sym_pair_tiles = 0, axpy_pair_tiles = 0;
 };
@@ -149,17 +149,19 @@ muon_status encode_f32_map(EncodeTiledFn enc, CUtensorMap* map, float* base, int
 }
 
 // CTA-pair tiling: Gram/poly tiles per matrix (column pairs q, row pairs 0..q) and their
-// executed flops; axpy tiles per matrix (row pairs x 256-column tiles).
+// executed flops; axpy tiles per matrix (row pairs x 256-column tiles).  A row pair whose
+// second block does not exist (odd row_blocks, last pair) runs as M = 128 tiles.
 int pair_col_pairs(int row_blocks) { return (row_blocks + 1) / 2; }
 int pair_sym_tiles(int row_blocks) {
     const int Q = pair_col_pairs(row_blocks);
     return Q * (Q + 1) / 2;
 }
+double pair_rows(int row_blocks, int rp) { return 2 * rp + 1 < row_blocks ? 256.0 : 128.0; }
 double pair_sym_exec_flops(int row_blocks, int K) {
     double f = 0.0;
     for (int q = 0; q < pair_col_pairs(row_blocks); ++q) {
         const int ncols = (2 * q + 1 < row_blocks) ? 256 : 128;
-        f += static_cast<double>(q + 1) * 2.0 * 256.0 * ncols * K;
+        for (int rp = 0; rp <= q; ++rp) f += 2.0 * pair_rows(row_blocks, rp) * ncols * K;
     }
     return f;
 }
@@ -167,7 +169,7 @@ double pair_axpy_exec_flops(int row_blocks, int n, int K) {
     double f = 0.0;
     for (int c0 = 0; c0 < n; c0 += 256) {
         const int ncols = (n - c0 > 128) ? 256 : 128;
-        f += static_cast<double>(pair_col_pairs(row_blocks)) * 2.0 * 256.0 * ncols * K;
+        for (int rp = 0; rp < pair_col_pairs(row_blocks); ++rp) f += 2.0 * pair_rows(row_blocks, rp) * ncols * K;
     }
     return f;
 }
@@ -313,6 +315,8 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
         }
         if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.tmAk64, bf, 2, cp.A, cp.m, cp.m, G, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st == MUON_OK)
+            st = encode_map_ex(ctx->encode, &cp.tmBk64, bf, 2, cp.B, cp.m, cp.m, G, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.epiA, bf, 2, cp.A, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         if (st == MUON_OK)
@@ -790,6 +794,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                             C.k_blocks = (cp.n + kPairBK - 1) / kPairBK;
                             pp.tmA[k] = cp.tmXk[pin];
                             pp.tmB[k] = cp.tmXk64[pin];
+                            pp.tmA64[k] = cp.tmXk64[pin];
                             pp.tmIn[k] = cp.epiX[pin];
                             pp.tmOut[k] = cp.epiA;
                         } else if (mode == MODE_POLY) {
@@ -798,6 +803,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                             C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
                             pp.tmA[k] = cp.tmAk;
                             pp.tmB[k] = cp.tmAk64;
+                            pp.tmA64[k] = cp.tmAk64;
                             pp.tmIn[k] = cp.epiA;
                             pp.tmOut[k] = cp.epiB;
                         } else {
@@ -806,6 +812,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                             C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
                             pp.tmA[k] = cp.tmBk;
                             pp.tmB[k] = cp.tmXmn128[pin];
+                            pp.tmA64[k] = cp.tmBk64;
                             pp.tmIn[k] = cp.epiX[pin];
                             pp.tmOut[k] = cp.epiX[pout];
                         }

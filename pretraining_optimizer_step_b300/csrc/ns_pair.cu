@@ -33,6 +33,11 @@
 // diagonal block there is symmetric and stored whole, so either orientation of
 // it is correct).
 //   axpy:      tile = row blocks (2 rp, 2 rp + 1) x columns [256 ct, 256 ct + N).
+// Half tiles: when a matrix has an odd number of 128-row blocks, its last row pair has
+// one real block.  Those tiles run as M = 128 pair MMAs: each CTA loads 64 rows of that
+// block, and each CTA's 64 x N accumulator is folded into TMEM as lanes 0..63 = columns
+// [0, N/2), lanes 64..127 = columns [N/2, N), TMEM columns 0..N/2 - 1.  So every epilogue
+// warp takes 32 rows x N/2 columns.
 //
 // CTA layout (192 threads, persistent over the pair tiles):
 //   warp 0      TMA producer (both CTAs): ring of 3 stages (2 in the final launch when it
@@ -61,7 +66,10 @@ namespace {
 struct PairTile {
     int ci;      // class
     int mat;     // matrix within the class
-    int rb;      // this CTA's row block (128 rows)
+    int rb0;     // the pair's first row block
+    int rb;      // this CTA's row block (128 rows; a half tile's single block for both CTAs)
+    int row0;    // this CTA's first oriented row: rb * 128, or in a half tile rb0 * 128 + 64 rank
+    int half_m;  // M = 128 tile (the pair's second row block does not exist)
     int c0;      // first output column of the tile
     int ncols;   // N: 256 or 128
 };
@@ -83,16 +91,19 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& P, int t,
             ++q;
         }
         const int rp = lt - base;
-        pt.rb = 2 * rp + rank;
+        pt.rb0 = 2 * rp;
         pt.c0 = 256 * q;
         pt.ncols = (2 * q + 1 < C.row_blocks) ? 256 : 128;
     } else {
         const int rp = lt / C.col_groups;
         const int ct = lt - rp * C.col_groups;
-        pt.rb = 2 * rp + rank;
+        pt.rb0 = 2 * rp;
         pt.c0 = 256 * ct;
         pt.ncols = (C.n - pt.c0 > 128) ? 256 : 128;
     }
+    pt.half_m = pt.rb0 + 1 >= C.row_blocks ? 1 : 0;
+    pt.rb = pt.half_m ? pt.rb0 : pt.rb0 + rank;
+    pt.row0 = pt.half_m ? pt.rb0 * 128 + 64 * rank : pt.rb * 128;
     return pt;
 }
 
@@ -196,14 +207,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int b0 = pt.c0 + rank * half;         // first of them
             // symmetric operands read from upper-block storage: first row / column block of the pair
             const bool a_symm = P.mode != MODE_GRAM;    // poly: A; axpy: B'
-            const int a_first = pt.rb - rank;           // the pair's first row block
+            const int a_first = pt.rb0;                 // the pair's first row block
             const int b_first = pt.c0 >> 7;             // the pair's first column block (poly)
+            const uint32_t a_bytes = pt.half_m ? 16384u : 32768u;  // this CTA's A rows x 128 K
             // a diagonal tile of a symmetric product with N = 256: each CTA's half of the B operand is
             // its own A panel (same rows, K block and orientation), so only the A panels are loaded
             const bool diag = sym && pt.ncols == 256 && b_first == a_first;
             const uint32_t total_bytes =
-                diag ? 2u * 2u * kPairPanelBytes
-                     : 2u * (2u * kPairPanelBytes + static_cast<uint32_t>(half) * kPairBK * 2u);
+                diag ? 2u * a_bytes : 2u * (a_bytes + static_cast<uint32_t>(half) * kPairBK * 2u);
             for (int kb = 0; kb < C.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, &abort_flag, P.timeout_ns)) {
                     latch_status(P.status, STATUS_TIMEOUT);
@@ -218,13 +229,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 if (leader) mbar_arrive_expect_tx(&full_bar[stage], total_bytes);
                 const bool a_tr = a_symm && kb <= a_first;   // this K block is below the stored triangle
                 for (int h = 0; h < 2; ++h) {
+                    if (a_tr && pt.half_m && h == 1) break;  // a half tile's 64 rows are one MN-major panel
                     if (P.inject_lost_load && leader && !injected && cluster == 0) {
                         injected = true;  // test hook: this A panel never arrives
                     } else if (a_tr) {
                         // MN-major: 64 of this CTA's rows (as columns of the stored block) x 128 K rows
-                        tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, pt.rb * 128 + 64 * h, k0, pt.mat);
+                        tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, pt.row0 + 64 * h, k0, pt.mat);
+                    } else if (pt.half_m) {
+                        // K-major, 64 rows: box 64 (K) x 64 rows
+                        tma_load_3d_pair(sa + h * kPairPanelBytes, &P.tmA64[pt.ci], bar, k0 + 64 * h, pt.row0, pt.mat);
                     } else {
-                        tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, k0 + 64 * h, pt.rb * 128, pt.mat);
+                        tma_load_3d_pair(sa + h * kPairPanelBytes, mA, bar, k0 + 64 * h, pt.row0, pt.mat);
                     }
                 }
                 if (diag) {
@@ -264,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const PairTile pt = decode_pair_tile(P, t, 0, sym);
             const PairClass& C = P.cls[pt.ci];
             const bool a_symm = P.mode != MODE_GRAM;
-            const int a_first = pt.rb;            // rank 0's row block = the pair's first
+            const int a_first = pt.rb0;           // the pair's first row block
             const int b_first = pt.c0 >> 7;
             const bool diag = sym && pt.ncols == 256 && b_first == a_first;  // B halves = A panels
             if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_flag, P.timeout_ns)) {
@@ -286,7 +301,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const uint32_t sb = diag ? sa : sa + 2 * kPairPanelBytes;
                 const int a_mn = (a_symm && kb <= a_first) ? 1 : 0;
                 const int b_mn = sym ? ((P.mode == MODE_POLY && kb <= b_first) ? 1 : 0) : 1;
-                const uint32_t idesc = idesc_bf16_f32_ab(256, pt.ncols, a_mn, b_mn);
+                const uint32_t idesc = idesc_bf16_f32_ab(pt.half_m ? 128 : 256, pt.ncols, a_mn, b_mn);
 #pragma unroll
                 for (int kk = 0; kk < kPairBK / 16; ++kk) {
                     // K-major: K panel kk / 4, 32 B per 16 of K; MN-major: 64-wide atoms 16 KiB apart,
@@ -347,23 +362,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const PairTile pt = decode_pair_tile(P, t, rank, sym);
             const PairClass& C = P.cls[pt.ci];
             const int gm = C.mat_base + pt.mat;
-            const int grow0 = pt.rb * 128 + lg * 32;        // first oriented row of this warp
+            // this warp's 32 rows and first column: a half tile folds each CTA's 64 rows x N columns
+            // into lanes 0..63 (columns [0, N/2)) and 64..127 (columns [N/2, N))
+            const int grow0 = pt.row0 + (pt.half_m ? (lg & 1) * 32 : lg * 32);  // first oriented row
+            const int cb = pt.half_m ? (lg >> 1) * (pt.ncols >> 1) : 0;          // column offset in the tile
             const bool warp_rows = pt.rb < C.row_blocks && grow0 < C.m;
             const int climit = sym ? C.m : C.n;
-            const int nch = pt.ncols / 32;
+            const int nch = pt.half_m ? pt.ncols / 64 : pt.ncols / 32;
             const bool transposed = C.transposed != 0;
             const CUtensorMap* pmap = final_mode ? &P.p_maps[gm] : nullptr;
             // a chunk is live when this warp has rows, its columns exist, and (Gram/poly) its
             // 128-column block is not below the diagonal for this row block
             auto live = [&](int ch) {
-                const int cc0 = pt.c0 + ch * 32;
+                const int cc0 = pt.c0 + cb + ch * 32;
                 if (!warp_rows || cc0 >= climit) return false;
                 if (sym && (cc0 >> 7) < pt.rb) return false;
                 return true;
             };
             auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0 (polynomial: the A tile)
                 const int slot = ch % n_in;
-                const int cc0 = pt.c0 + ch * 32;
+                const int cc0 = pt.c0 + cb + ch * 32;
                 mbar_arrive_expect_tx(&ibar[slot], 2048u);
                 tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 in_pending_bits |= 1u << slot;
@@ -398,7 +416,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const int slot = n_in > 0 ? ch % n_in : 0;
                 const bool lv = live(ch);
                 if (lv) {
-                    const int cc0 = pt.c0 + ch * 32;
+                    const int cc0 = pt.c0 + cb + ch * 32;
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw_v[j]);

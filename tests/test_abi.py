@@ -72,28 +72,31 @@ def enumerate_pair_tiles(m, n):
     (those that exist), rp <= q.  Every 128 x 128 block on or above the diagonal
     must be stored by exactly one tile (the lower block of a diagonal tile is not
     stored).  Axpy: tile (rp, ct) = row blocks 2rp, 2rp+1 x 256 columns from
-    256 ct (128 when fewer than 129 remain).  Returns tile counts and the executed
-    flops per unit K (2 x 256 x N per tile)."""
+    256 ct (128 when fewer than 129 remain).  A tile whose second row block does
+    not exist computes 128 rows (M = 128), every other 256.  Returns tile counts
+    and the executed flops per unit K (2 x rows x N per tile)."""
     rb = math.ceil(m / 128)
-    sym, sym_cols = [], 0
+    sym, sym_f = [], 0
     stored = set()
     for q in range(math.ceil(rb / 2)):
         cols = [c for c in (2 * q, 2 * q + 1) if c < rb]
         for rp in range(q + 1):
             sym.append((rp, q))
-            sym_cols += 128 * len(cols)
+            rows = 256 if 2 * rp + 1 < rb else 128
+            sym_f += 2 * rows * 128 * len(cols)
             for i in (2 * rp, 2 * rp + 1):
                 for c in cols:
                     if i < rb and i <= c:
                         assert (i, c) not in stored
                         stored.add((i, c))
     assert stored == {(i, j) for i in range(rb) for j in range(i, rb)}
-    axpy, axpy_cols = 0, 0
+    axpy, axpy_f = 0, 0
     for rp in range(math.ceil(rb / 2)):
+        rows = 256 if 2 * rp + 1 < rb else 128
         for c0 in range(0, n, 256):
             axpy += 1
-            axpy_cols += 256 if n - c0 > 128 else 128
-    return len(sym), axpy, 2 * 256 * sym_cols, 2 * 256 * axpy_cols
+            axpy_f += 2 * rows * (256 if n - c0 > 128 else 128)
+    return len(sym), axpy, sym_f, axpy_f
 
 
 def expected_plan(shapes, K):
