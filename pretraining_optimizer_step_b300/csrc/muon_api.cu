@@ -716,163 +716,161 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
 
     // ---- Newton-Schulz iterations: per group of <= kMaxClasses classes
     const int nclass = static_cast<int>(P->classes.size());
-    {
-        // fp32 weight maps of the fused update: re-encoded only when the params change
-        // (the NorMuon pass updates the weights in its own kernel)
-        bool changed = false;
-        for (int i = 0; i < n_mats && !changed && !nm; ++i) changed = P->mapped_p[i] != params[i];
-        if (changed) {
-            std::vector<CUtensorMap> pm(n_mats);
-            for (int k = 0; k < n_mats; ++k) {
-                const int i = P->order[k];
-                if (encode_f32_map(ctx->encode, &pm[k], params[i], shapes[i].rows, shapes[i].cols) != MUON_OK)
-                    return MUON_ERR_CUDA;
-            }
-            // launches already enqueued, on any stream, may still read the previous maps
-            if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
-            if (cudaMemcpy(P->p_maps, pm.data(), n_mats * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
+    // fp32 weight maps of the fused update: re-encoded only when the params change
+    // (the NorMuon pass updates the weights in its own kernel)
+    bool changed = false;
+    for (int i = 0; i < n_mats && !changed && !nm; ++i) changed = P->mapped_p[i] != params[i];
+    if (changed) {
+        std::vector<CUtensorMap> pm(n_mats);
+        for (int k = 0; k < n_mats; ++k) {
+            const int i = P->order[k];
+            if (encode_f32_map(ctx->encode, &pm[k], params[i], shapes[i].rows, shapes[i].cols) != MUON_OK)
                 return MUON_ERR_CUDA;
-            P->mapped_p.assign(params, params + n_mats);
         }
-        static PairParams pp;  // ~5 KiB: kept off the stack
-        // step position of every class's first matrix (positions are class-ordered)
-        std::vector<int> class_base(nclass, 0);
-        for (int c = 1; c < nclass; ++c)
-            class_base[c] = class_base[c - 1] + static_cast<int>(P->classes[c - 1].mats.size());
-        for (int it = 0; it < ns_steps; ++it) {
-            const double* row = &ctx->coeffs[3 * it];
-            const int pin = it & 1, pout = pin ^ 1;
-            const bool last = (it == ns_steps - 1);
-            for (int g0 = 0; g0 < nclass; g0 += kMaxClasses) {
-                const int gc = std::min(kMaxClasses, nclass - g0);
-                for (int mode = MODE_GRAM; mode <= MODE_AXPY; ++mode) {
-                    std::memset(&pp, 0, sizeof(pp));
-                    const int eff_mode =
-                        (mode == MODE_AXPY && last) ? (nm ? MODE_AXPY_O : MODE_AXPY_FINAL) : mode;
-                    pp.mode = eff_mode;
-                    pp.nclasses = gc;
-                    pp.first_iter = (it == 0 && mode != MODE_POLY) ? 1 : 0;
-                    pp.ca = static_cast<float>(row[0]);
-                    pp.cb = static_cast<float>(row[1]);
-                    pp.cc = static_cast<float>(row[2]);
-                    pp.inv_norm = P->inv_norm;
-                    pp.aspect = P->aspect;
-                    pp.lr = lr;
-                    pp.p_maps = P->p_maps;
-                    pp.dbg_maps = keep_o ? P->dbg_maps : nullptr;
-                    pp.o_maps = P->o_maps;
-                    pp.status = ctx->status;
-                    pp.timeout_ns = ctx->timeout_ns;
-                    pp.inject_lost_load = ((ctx->debug & MUON_DEBUG_INJECT_LOST_LOAD) && !ctx->injected &&
-                                           it == 0 && mode == MODE_GRAM && g0 == 0)
-                                              ? 1
-                                              : 0;
-                    if (pp.inject_lost_load) ctx->injected = true;
-                    // The clusters take tiles round-robin in launch order, so the classes whose tiles
-                    // run longest (deepest K) go first and the last wave is made of the shortest
-                    // tiles; within a class the tiles of one matrix stay adjacent (their operands
-                    // share L2).
-                    int ord[kMaxClasses];
-                    for (int k = 0; k < gc; ++k) ord[k] = g0 + k;
-                    auto depth = [&](int c) { return mode == MODE_GRAM ? P->classes[c].n : P->classes[c].m; };
-                    std::stable_sort(ord, ord + gc, [&](int x, int y) { return depth(x) > depth(y); });
-                    int tiles = 0;
-                    for (int k = 0; k < gc; ++k) {
-                        const ClassPlan& cp = P->classes[ord[k]];
-                        PairClass& C = pp.cls[k];
-                        const int G = static_cast<int>(cp.mats.size());
-                        C.m = cp.m;
-                        C.n = cp.n;
-                        C.nmats = G;
-                        C.tile_begin = tiles;
-                        C.row_blocks = cp.row_blocks;
-                        C.transposed = cp.transposed;
-                        C.mat_base = class_base[ord[k]];
-                        if (mode == MODE_GRAM) {
-                            C.tiles_per_mat = cp.sym_pair_tiles;
-                            C.col_groups = cp.col_pairs;
-                            C.k_blocks = (cp.n + kPairBK - 1) / kPairBK;
-                            pp.tmA[k] = cp.tmXk[pin];
-                            pp.tmB[k] = cp.tmXk64[pin];
-                            pp.tmA64[k] = cp.tmXk64[pin];
-                            pp.tmIn[k] = cp.epiX[pin];
-                            pp.tmOut[k] = cp.epiA;
-                        } else if (mode == MODE_POLY) {
-                            C.tiles_per_mat = cp.sym_pair_tiles;
-                            C.col_groups = cp.col_pairs;
-                            C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
-                            pp.tmA[k] = cp.tmAk;
-                            pp.tmB[k] = cp.tmAk64;
-                            pp.tmA64[k] = cp.tmAk64;
-                            pp.tmIn[k] = cp.epiA;
-                            pp.tmOut[k] = cp.epiB;
-                        } else {
-                            C.tiles_per_mat = cp.axpy_pair_tiles;
-                            C.col_groups = cp.col_tiles;
-                            C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
-                            pp.tmA[k] = cp.tmBk;
-                            pp.tmB[k] = cp.tmXmn128[pin];
-                            pp.tmA64[k] = cp.tmBk64;
-                            pp.tmIn[k] = cp.epiX[pin];
-                            pp.tmOut[k] = cp.epiX[pout];
-                        }
-                        tiles += C.tiles_per_mat * G;
-                    }
-                    pp.total_tiles = tiles;
-                    const int clusters = std::min(tiles, ctx->max_clusters);
-                    const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3
-                                     : eff_mode == MODE_AXPY_O ? 6 : 4;
-                    const muon_status st =
-                        timed_launch(ctx, kind, stream, [&] { return launch_ns_pair(pp, clusters, stream); });
-                    if (st != MUON_OK) return st;
-                }
-            }
-        }
-        if (nm) {
-            // ---- NorMuon: per-row statistics and ratio, then the weight update
-            static NormuonParams np;  // ~12 KiB: kept off the stack
-            for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
-                const int cnt = std::min(kMomentumMaxMats, n_mats - base);
-                std::memset(&np, 0, sizeof(np));
-                int ctas = 0, tiles = 0;
-                for (int k = 0; k < cnt; ++k) {
-                    const int pos = base + k;
-                    const int i = P->order[pos];
-                    NormuonMat& M = np.mats[k];
-                    M.O = P->o_bufs[i];
-                    M.V = nm->second_moments[i];
-                    M.p = params[i];
-                    M.dbg = keep_o ? P->dbg_O[i] : nullptr;
-                    M.rows = shapes[i].rows;
-                    M.cols = shapes[i].cols;
-                    M.cta_begin = ctas;
-                    M.nctas = (M.rows + kNormRowsPerCta - 1) / kNormRowsPerCta;
-                    M.tile_begin = tiles;
-                    M.tiles_x = (M.cols + 63) / 64;
-                    M.pos = pos;
-                    ctas += M.nctas;
-                    tiles += M.tiles_x * ((M.rows + 63) / 64);
-                }
-                np.nmats = cnt;
-                np.beta2 = nm->beta2;
-                np.eps = nm->eps;
-                np.lr = lr;
-                np.aspect = P->aspect;
-                np.step = P->nm_step;
-                np.row_base = P->nm_row_base;
-                np.partials = P->nm_partials;
-                np.counters = P->nm_counters;
-                np.ratio = P->nm_ratio;
-                np.total = ctas;
-                muon_status st = timed_launch(ctx, 7, stream, [&] { return launch_normuon_rows(np, stream); });
-                if (st != MUON_OK) return st;
-                np.total = tiles;
-                st = timed_launch(ctx, 7, stream, [&] { return launch_normuon_update(np, stream); });
-                if (st != MUON_OK) return st;
-            }
-        }
-        return MUON_OK;
+        // launches already enqueued, on any stream, may still read the previous maps
+        if (cudaDeviceSynchronize() != cudaSuccess) return MUON_ERR_CUDA;
+        if (cudaMemcpy(P->p_maps, pm.data(), n_mats * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
+            return MUON_ERR_CUDA;
+        P->mapped_p.assign(params, params + n_mats);
     }
+    static PairParams pp;  // ~5 KiB: kept off the stack
+    // step position of every class's first matrix (positions are class-ordered)
+    std::vector<int> class_base(nclass, 0);
+    for (int c = 1; c < nclass; ++c)
+        class_base[c] = class_base[c - 1] + static_cast<int>(P->classes[c - 1].mats.size());
+    for (int it = 0; it < ns_steps; ++it) {
+        const double* row = &ctx->coeffs[3 * it];
+        const int pin = it & 1, pout = pin ^ 1;
+        const bool last = (it == ns_steps - 1);
+        for (int g0 = 0; g0 < nclass; g0 += kMaxClasses) {
+            const int gc = std::min(kMaxClasses, nclass - g0);
+            for (int mode = MODE_GRAM; mode <= MODE_AXPY; ++mode) {
+                std::memset(&pp, 0, sizeof(pp));
+                const int eff_mode =
+                    (mode == MODE_AXPY && last) ? (nm ? MODE_AXPY_O : MODE_AXPY_FINAL) : mode;
+                pp.mode = eff_mode;
+                pp.nclasses = gc;
+                pp.first_iter = (it == 0 && mode != MODE_POLY) ? 1 : 0;
+                pp.ca = static_cast<float>(row[0]);
+                pp.cb = static_cast<float>(row[1]);
+                pp.cc = static_cast<float>(row[2]);
+                pp.inv_norm = P->inv_norm;
+                pp.aspect = P->aspect;
+                pp.lr = lr;
+                pp.p_maps = P->p_maps;
+                pp.dbg_maps = keep_o ? P->dbg_maps : nullptr;
+                pp.o_maps = P->o_maps;
+                pp.status = ctx->status;
+                pp.timeout_ns = ctx->timeout_ns;
+                pp.inject_lost_load = ((ctx->debug & MUON_DEBUG_INJECT_LOST_LOAD) && !ctx->injected &&
+                                       it == 0 && mode == MODE_GRAM && g0 == 0)
+                                          ? 1
+                                          : 0;
+                if (pp.inject_lost_load) ctx->injected = true;
+                // The clusters take tiles round-robin in launch order, so the classes whose tiles
+                // run longest (deepest K) go first and the last wave is made of the shortest
+                // tiles; within a class the tiles of one matrix stay adjacent (their operands
+                // share L2).
+                int ord[kMaxClasses];
+                for (int k = 0; k < gc; ++k) ord[k] = g0 + k;
+                auto depth = [&](int c) { return mode == MODE_GRAM ? P->classes[c].n : P->classes[c].m; };
+                std::stable_sort(ord, ord + gc, [&](int x, int y) { return depth(x) > depth(y); });
+                int tiles = 0;
+                for (int k = 0; k < gc; ++k) {
+                    const ClassPlan& cp = P->classes[ord[k]];
+                    PairClass& C = pp.cls[k];
+                    const int G = static_cast<int>(cp.mats.size());
+                    C.m = cp.m;
+                    C.n = cp.n;
+                    C.nmats = G;
+                    C.tile_begin = tiles;
+                    C.row_blocks = cp.row_blocks;
+                    C.transposed = cp.transposed;
+                    C.mat_base = class_base[ord[k]];
+                    if (mode == MODE_GRAM) {
+                        C.tiles_per_mat = cp.sym_pair_tiles;
+                        C.col_groups = cp.col_pairs;
+                        C.k_blocks = (cp.n + kPairBK - 1) / kPairBK;
+                        pp.tmA[k] = cp.tmXk[pin];
+                        pp.tmB[k] = cp.tmXk64[pin];
+                        pp.tmA64[k] = cp.tmXk64[pin];
+                        pp.tmIn[k] = cp.epiX[pin];
+                        pp.tmOut[k] = cp.epiA;
+                    } else if (mode == MODE_POLY) {
+                        C.tiles_per_mat = cp.sym_pair_tiles;
+                        C.col_groups = cp.col_pairs;
+                        C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
+                        pp.tmA[k] = cp.tmAk;
+                        pp.tmB[k] = cp.tmAk64;
+                        pp.tmA64[k] = cp.tmAk64;
+                        pp.tmIn[k] = cp.epiA;
+                        pp.tmOut[k] = cp.epiB;
+                    } else {
+                        C.tiles_per_mat = cp.axpy_pair_tiles;
+                        C.col_groups = cp.col_tiles;
+                        C.k_blocks = (cp.m + kPairBK - 1) / kPairBK;
+                        pp.tmA[k] = cp.tmBk;
+                        pp.tmB[k] = cp.tmXmn128[pin];
+                        pp.tmA64[k] = cp.tmBk64;
+                        pp.tmIn[k] = cp.epiX[pin];
+                        pp.tmOut[k] = cp.epiX[pout];
+                    }
+                    tiles += C.tiles_per_mat * G;
+                }
+                pp.total_tiles = tiles;
+                const int clusters = std::min(tiles, ctx->max_clusters);
+                const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3
+                                 : eff_mode == MODE_AXPY_O ? 6 : 4;
+                const muon_status st =
+                    timed_launch(ctx, kind, stream, [&] { return launch_ns_pair(pp, clusters, stream); });
+                if (st != MUON_OK) return st;
+            }
+        }
+    }
+    if (nm) {
+        // ---- NorMuon: per-row statistics and ratio, then the weight update
+        static NormuonParams np;  // ~12 KiB: kept off the stack
+        for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
+            const int cnt = std::min(kMomentumMaxMats, n_mats - base);
+            std::memset(&np, 0, sizeof(np));
+            int ctas = 0, tiles = 0;
+            for (int k = 0; k < cnt; ++k) {
+                const int pos = base + k;
+                const int i = P->order[pos];
+                NormuonMat& M = np.mats[k];
+                M.O = P->o_bufs[i];
+                M.V = nm->second_moments[i];
+                M.p = params[i];
+                M.dbg = keep_o ? P->dbg_O[i] : nullptr;
+                M.rows = shapes[i].rows;
+                M.cols = shapes[i].cols;
+                M.cta_begin = ctas;
+                M.nctas = (M.rows + kNormRowsPerCta - 1) / kNormRowsPerCta;
+                M.tile_begin = tiles;
+                M.tiles_x = (M.cols + 63) / 64;
+                M.pos = pos;
+                ctas += M.nctas;
+                tiles += M.tiles_x * ((M.rows + 63) / 64);
+            }
+            np.nmats = cnt;
+            np.beta2 = nm->beta2;
+            np.eps = nm->eps;
+            np.lr = lr;
+            np.aspect = P->aspect;
+            np.step = P->nm_step;
+            np.row_base = P->nm_row_base;
+            np.partials = P->nm_partials;
+            np.counters = P->nm_counters;
+            np.ratio = P->nm_ratio;
+            np.total = ctas;
+            muon_status st = timed_launch(ctx, 7, stream, [&] { return launch_normuon_rows(np, stream); });
+            if (st != MUON_OK) return st;
+            np.total = tiles;
+            st = timed_launch(ctx, 7, stream, [&] { return launch_normuon_update(np, stream); });
+            if (st != MUON_OK) return st;
+        }
+    }
+    return MUON_OK;
 }
 
 muon_status muon_step(float* const params[], const float* const grads[], float* const momentum_bufs[],
