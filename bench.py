@@ -177,7 +177,7 @@ class ClockSampler:
 # launch, averaged with a step's launch counts (4, 5, 5, 1) and scaled by 13; and the sha256
 # of the kernel source it was taken on.  The figure is reported only while the source is
 # unchanged.
-NS_PAIR_TRAFFIC = {"bytes_per_launch_d26": 2.3745e+09, "source_sha256": "867309879dc16fecdc3ac2ad7e079f92accf0cd291d101e9a0a3a2bbc5c42535"}
+NS_PAIR_TRAFFIC = {"bytes_per_launch_d26": 2.4111e+09, "source_sha256": "20c426210094aad8039101d84c76f7cb808daad214ea9f9d4b0784a32d8202af"}
 
 
 def ns_pair_traffic():
