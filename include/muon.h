@@ -67,7 +67,8 @@ typedef enum muon_status {
     MUON_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed */
     MUON_ERR_OUT_OF_MEMORY = 6,       /* workspace allocation failed */
     MUON_ERR_DEVICE_TIMEOUT = 7,      /* a kernel's bounded wait expired (device status) */
-    MUON_ERR_DEVICE_BOUNDS = 8,       /* a kernel saw an out-of-range tile (device status) */
+    MUON_ERR_DEVICE_BOUNDS = 8,       /* a kernel refused launch parameters whose tile list does not
+                                         match its classes (device status; that launch ran no tile) */
     MUON_ERR_UNSUPPORTED_DEVICE = 9,  /* no device, or the current device is not sm_103 */
     MUON_ERR_SCRATCH_LIMIT = 10       /* the request needs more than the fixed scratch of
                                          muon_momentum_norm_noalloc holds */
@@ -88,9 +89,13 @@ enum {
     MUON_DEBUG_KEEP_O = 1,            /* also write O (fp32, stored layout) for muon_debug_copy_ns_output */
     MUON_DEBUG_POISON_WORKSPACE = 2,  /* fill the bf16 workspace with NaN before every step */
     MUON_DEBUG_TIME_KERNELS = 4,      /* record CUDA events around every launch (muon_kernel_times) */
-    MUON_DEBUG_INJECT_LOST_LOAD = 8   /* test hook: one operand load of the first Gram launch is never
+    MUON_DEBUG_INJECT_LOST_LOAD = 8,  /* test hook: one operand load of the first Gram launch is never
                                          issued, so the consumer's bounded wait must expire and the step
                                          reports MUON_ERR_DEVICE_TIMEOUT; the result is then invalid */
+    MUON_DEBUG_INJECT_BAD_TILES = 16  /* test hook: the first Gram launch is given one tile more than its
+                                         classes hold; the kernel's parameter check must refuse it (no
+                                         tile runs) and the step reports MUON_ERR_DEVICE_BOUNDS; the
+                                         result is then invalid */
 };
 
 typedef struct muon_config {

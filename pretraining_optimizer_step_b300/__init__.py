@@ -38,6 +38,7 @@ MUON_DEBUG_KEEP_O = 1
 MUON_DEBUG_POISON_WORKSPACE = 2
 MUON_DEBUG_TIME_KERNELS = 4
 MUON_DEBUG_INJECT_LOST_LOAD = 8
+MUON_DEBUG_INJECT_BAD_TILES = 16
 
 # The five per-iteration "Polar Express" (a, b, c) rows, for muon_init(coeffs=...).  The pages
 # print the first two to three decimals (apidog.com "Cara Melatih ChatGPT Sendiri dengan Budget 50

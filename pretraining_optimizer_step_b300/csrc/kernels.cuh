@@ -11,7 +11,7 @@ namespace muon {
 // Device status word bits (latched with atomicOr, read by muon_get_status).
 enum : unsigned int {
     STATUS_TIMEOUT = 1u,
-    STATUS_BOUNDS = 2u,
+    STATUS_BOUNDS = 2u,     // a launch's tile list did not match its classes (no tile was run)
 };
 
 // ------------------------------------------------------------------ momentum + norm

@@ -11,6 +11,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/muon.h"
 #include "kernels.cuh"
 
@@ -101,9 +103,25 @@ struct Context {
     double kind_ms[kKinds] = {0};
     int kind_launches[kKinds] = {0};
     bool injected = false;
+    bool injected_bad = false;
 };
 
 Context* g_ctx = nullptr;
+
+// An NVTX range for the lifetime of a scope (header-only NVTX: a no-op unless a profiler
+// attaches).  The step, its momentum pass, every Newton-Schulz iteration and the NorMuon pass
+// show up as named ranges on the host timeline.
+struct NvtxScope {
+    explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+    NvtxScope(const NvtxScope&) = delete;
+    NvtxScope& operator=(const NvtxScope&) = delete;
+};
+const char* const kIterRange[kMaxCoeffRows] = {
+    "muon NS iteration 1",  "muon NS iteration 2",  "muon NS iteration 3",  "muon NS iteration 4",
+    "muon NS iteration 5",  "muon NS iteration 6",  "muon NS iteration 7",  "muon NS iteration 8",
+    "muon NS iteration 9",  "muon NS iteration 10", "muon NS iteration 11", "muon NS iteration 12",
+    "muon NS iteration 13", "muon NS iteration 14", "muon NS iteration 15", "muon NS iteration 16"};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -519,7 +537,7 @@ const char* muon_status_string(muon_status s) {
         case MUON_ERR_CUDA: return "CUDA call failed";
         case MUON_ERR_OUT_OF_MEMORY: return "workspace allocation failed";
         case MUON_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
-        case MUON_ERR_DEVICE_BOUNDS: return "a kernel saw an out-of-range tile";
+        case MUON_ERR_DEVICE_BOUNDS: return "a kernel refused a tile list that does not match its classes";
         case MUON_ERR_UNSUPPORTED_DEVICE: return "no sm_103 CUDA device";
         case MUON_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of muon_momentum_norm_noalloc";
     }
@@ -628,6 +646,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
             return MUON_ERR_MISALIGNED;
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    NvtxScope step_range(nm ? "muon_step_normuon" : "muon_step");
 
     // the plan of this shape list: reused when cached (moved to the front), else built, dropping
     // the least recently used one when kMaxPlans are held
@@ -669,6 +688,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
 
     // ---- momentum + norm (chunks of kMomentumMaxMats matrices, class order)
     static MomentumParams mp;  // ~12 KiB: kept off the stack
+    nvtxRangePushA("muon momentum+norm");
     for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
         const int cnt = std::min(kMomentumMaxMats, n_mats - base);
         std::memset(&mp, 0, sizeof(mp));
@@ -688,8 +708,12 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
         mp.inv_norm = P->inv_norm;
         mp.norms = P->norms;
         const muon_status st = timed_launch(ctx, 0, stream, [&] { return launch_momentum_norm(mp, stream); });
-        if (st != MUON_OK) return st;
+        if (st != MUON_OK) {
+            nvtxRangePop();
+            return st;
+        }
     }
+    nvtxRangePop();
 
     const bool keep_o = (ctx->debug & MUON_DEBUG_KEEP_O) != 0;
     if (ns_steps == 0) {
@@ -739,6 +763,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
     for (int c = 1; c < nclass; ++c)
         class_base[c] = class_base[c - 1] + static_cast<int>(P->classes[c - 1].mats.size());
     for (int it = 0; it < ns_steps; ++it) {
+        NvtxScope iter_range(kIterRange[it]);
         const double* row = &ctx->coeffs[3 * it];
         const int pin = it & 1, pout = pin ^ 1;
         const bool last = (it == ns_steps - 1);
@@ -767,6 +792,9 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                                           ? 1
                                           : 0;
                 if (pp.inject_lost_load) ctx->injected = true;
+                const bool bad_tiles = (ctx->debug & MUON_DEBUG_INJECT_BAD_TILES) && !ctx->injected_bad && it == 0 &&
+                                       mode == MODE_GRAM && g0 == 0;
+                if (bad_tiles) ctx->injected_bad = true;
                 // The clusters take tiles round-robin in launch order, so the classes whose tiles
                 // run longest (deepest K) go first and the last wave is made of the shortest
                 // tiles; within a class the tiles of one matrix stay adjacent (their operands
@@ -817,7 +845,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                     }
                     tiles += C.tiles_per_mat * G;
                 }
-                pp.total_tiles = tiles;
+                pp.total_tiles = bad_tiles ? tiles + 1 : tiles;
                 const int clusters = std::min(tiles, ctx->max_clusters);
                 const int kind = eff_mode == MODE_GRAM ? 1 : eff_mode == MODE_POLY ? 2 : eff_mode == MODE_AXPY ? 3
                                  : eff_mode == MODE_AXPY_O ? 6 : 4;
@@ -829,6 +857,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
     }
     if (nm) {
         // ---- NorMuon: per-row statistics and ratio, then the weight update
+        NvtxScope nm_range("muon NorMuon rows+update");
         static NormuonParams np;  // ~12 KiB: kept off the stack
         for (int base = 0; base < n_mats; base += kMomentumMaxMats) {
             const int cnt = std::min(kMomentumMaxMats, n_mats - base);

@@ -162,6 +162,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int cluster = static_cast<int>(cluster_id_x());
     const int nclusters = static_cast<int>(cluster_count_x());
     const bool sym = (P.mode == MODE_GRAM || P.mode == MODE_POLY);
+    // The launch's tile list must be the one its classes describe (consecutive, non-empty
+    // classes whose tile counts add up to total_tiles).  Every CTA checks the same parameters
+    // and reaches the same verdict; on a mismatch the status word gets STATUS_BOUNDS and
+    // every role's tile loop is empty, so no tile is decoded out of range and every role
+    // still reaches the exit barrier.
+    int expect_tiles = 0;
+    bool params_ok = P.nclasses >= 1 && P.nclasses <= kMaxClasses && P.total_tiles >= 0;
+    for (int c = 0; params_ok && c < P.nclasses; ++c) {
+        const PairClass& C = P.cls[c];
+        params_ok = C.tile_begin == expect_tiles && C.nmats >= 1 && C.tiles_per_mat >= 1 && C.k_blocks >= 1 &&
+                    C.row_blocks >= 1 && C.m >= 8 && C.n >= C.m;
+        expect_tiles += C.tiles_per_mat * C.nmats;
+    }
+    params_ok = params_ok && expect_tiles == P.total_tiles;
+    const int total_tiles = params_ok ? P.total_tiles : 0;
+    if (!params_ok && threadIdx.x == 0 && cluster_ctarank() == 0 && cluster_id_x() == 0)
+        atomicOr(P.status, STATUS_BOUNDS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairMaxStages; ++s) {
@@ -198,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         uint32_t phase = 0;
         bool aborted = false;
         bool injected = false;
-        for (int t = cluster; t < P.total_tiles && !aborted; t += nclusters) {
+        for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
             const PairTile pt = decode_pair_tile(P, t, rank, sym);
             const PairClass& C = P.cls[pt.ci];
             const CUtensorMap* mA = &P.tmA[pt.ci];
@@ -275,7 +292,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool aborted = false;
-        for (int t = cluster; t < P.total_tiles && !aborted; t += nclusters) {
+        bool issued = false;  // any MMA issued (only then is there anything to drain)
+        for (int t = cluster; t < total_tiles && !aborted; t += nclusters) {
             const PairTile pt = decode_pair_tile(P, t, 0, sym);
             const PairClass& C = P.cls[pt.ci];
             const bool a_symm = P.mode != MODE_GRAM;
@@ -313,6 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                                 : smem_desc_sw128(sb + kpan, 16, 1024);
                     tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
+                issued = true;
                 tc_commit_pair_multicast(&empty_bar[stage], 0x3);
                 if (++stage == nstages) {
                     stage = 0;
@@ -327,8 +346,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             }
         }
         // every MMA issued must finish before TMEM is released
-        tc_commit_pair_multicast(&drain_bar, 0x1);
-        mbar_wait_bounded(&drain_bar, 0, nullptr, P.timeout_ns);
+        if (issued) {
+            tc_commit_pair_multicast(&drain_bar, 0x1);
+            mbar_wait_bounded(&drain_bar, 0, nullptr, P.timeout_ns);
+        }
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int lg = warp & 3;                       // TMEM lane group of this warp
@@ -358,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool stores_issued = false;
-        for (int t = cluster; t < P.total_tiles; t += nclusters) {
+        for (int t = cluster; t < total_tiles; t += nclusters) {
             const PairTile pt = decode_pair_tile(P, t, rank, sym);
             const PairClass& C = P.cls[pt.ci];
             const int gm = C.mat_base + pt.mat;
