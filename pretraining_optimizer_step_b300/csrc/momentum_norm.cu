@@ -13,6 +13,7 @@
 // update_kernel: the weight update p -= lr sqrt(max(1, r/c)) O for ns_steps = 0,
 //   where O = X0 / (||u|| + eps).
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace muon {
 
@@ -45,6 +46,9 @@ __global__ void __launch_bounds__(kMomThreads)
     __shared__ float warp_sums[kMomThreads / 32];
     __shared__ double warp_sums_d[kMomThreads / 32];
     __shared__ int is_last;
+    // the first Gram launch (launched for programmatic serialization) may start launching once
+    // every CTA of this grid has started; it waits in its own prologue for this grid to finish
+    griddep_launch();
 
     const int t = blockIdx.x;
     const int mi = find_mat(P.mats, P.nmats, t);

@@ -56,6 +56,9 @@
 //               column access (transposes).
 // Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, raises its
 // abort flag, lets its own copies land, and joins the final cluster barrier.
+// Launches use programmatic dependent launch: a launch's CTAs take the SMs the previous
+// launch releases, run the prologue (barriers, TMEM, descriptor prefetch), and wait
+// (griddepcontrol.wait) for the previous grid before touching global memory.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -177,8 +180,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     params_ok = params_ok && expect_tiles == P.total_tiles;
     const int total_tiles = params_ok ? P.total_tiles : 0;
-    if (!params_ok && threadIdx.x == 0 && cluster_ctarank() == 0 && cluster_id_x() == 0)
-        atomicOr(P.status, STATUS_BOUNDS);
+    // The next launch on the stream (the next Newton-Schulz GEMM) may start launching now: its CTAs
+    // take SMs only as this grid's CTAs exit, and run their prologue while the last tiles finish.
+    griddep_launch();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairMaxStages; ++s) {
@@ -204,6 +208,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_slot;
+    // everything above touched only shared memory, TMEM and the launch parameters; the previous
+    // kernel's outputs (this launch's operands) and the buffers it read are safe from here on
+    griddep_wait();
+    if (!params_ok && threadIdx.x == 0 && rank == 0 && cluster == 0) atomicOr(P.status, STATUS_BOUNDS);
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -597,10 +605,22 @@ cudaError_t ns_pair_prepare(int* max_clusters) {
     return cudaSuccess;
 }
 
+// Launched with programmatic stream serialization: the CTAs of a launch that follows another
+// Newton-Schulz launch (or the momentum pass) start their prologue on SMs the previous grid has
+// released, and wait in the kernel for its completion.
 cudaError_t launch_ns_pair(const PairParams& p, int clusters, cudaStream_t s) {
     if (p.total_tiles <= 0 || clusters <= 0) return cudaSuccess;
-    ns_pair_kernel<<<2 * clusters, kGemmThreads, kPairSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ns_pair_kernel, p);
 }
 
 }  // namespace muon
