@@ -38,7 +38,7 @@ struct ClassPlan {
     // A-side K-major maps (box 64 x 128), B-side K-major maps (box 64 x 64), the MN-major X map
     // of the axpy B operand (box 64 x 128), and epilogue subtile maps (bf16 32 x 32)
     CUtensorMap tmXk[2], tmAk, tmBk;
-    CUtensorMap tmXk64[2], tmAk64, tmBk64, tmXmn128[2], epiX[2], epiA, epiB;
+    CUtensorMap tmXk64[2], tmAk64, tmBk64, tmXmn128[2], epiX[2], epiA, epiB, epiX64[2], epiA64;
     int row_blocks = 0, col_tiles = 0;
     int col_pairs = 0, sym_pair_tiles = 0, axpy_pair_tiles = 0;
 };
@@ -330,6 +330,9 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
             if (st == MUON_OK)
                 st = encode_map_ex(ctx->encode, &cp.epiX[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 32, 32,
                                    CU_TENSOR_MAP_SWIZZLE_64B);
+            if (st == MUON_OK)
+                st = encode_map_ex(ctx->encode, &cp.epiX64[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 64, 32,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
         }
         if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.tmAk64, bf, 2, cp.A, cp.m, cp.m, G, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -337,6 +340,8 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
             st = encode_map_ex(ctx->encode, &cp.tmBk64, bf, 2, cp.B, cp.m, cp.m, G, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.epiA, bf, 2, cp.A, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (st == MUON_OK)
+            st = encode_map_ex(ctx->encode, &cp.epiA64, bf, 2, cp.A, cp.m, cp.m, G, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.epiB, bf, 2, cp.B, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != MUON_OK) {
@@ -823,7 +828,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                         pp.tmB[k] = cp.tmXk64[pin];
                         pp.tmA64[k] = cp.tmXk64[pin];
                         pp.tmIn[k] = cp.epiX[pin];
-                        pp.tmOut[k] = cp.epiA;
+                        pp.tmOut[k] = cp.epiA64;
                     } else if (mode == MODE_POLY) {
                         C.tiles_per_mat = cp.sym_pair_tiles;
                         C.col_groups = cp.col_pairs;
@@ -841,7 +846,7 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                         pp.tmB[k] = cp.tmXmn128[pin];
                         pp.tmA64[k] = cp.tmBk64;
                         pp.tmIn[k] = cp.epiX[pin];
-                        pp.tmOut[k] = cp.epiX[pout];
+                        pp.tmOut[k] = cp.epiX64[pout];
                     }
                     tiles += C.tiles_per_mat * G;
                 }

@@ -368,15 +368,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // a slot is rewritten once the group that last read it -- n_out groups back -- has):
         //   final (8 KiB):   2 output slots of the fp32 32x32 weight change -lr s O
         //   final, debug copy of O (24 KiB): 2 output slot pairs {weight change, O} of 8 KiB
-        //   gram  (8 KiB):   4 output slots of bf16
+        //   gram, axpy (8 KiB): 2 output slots of bf16 32 x 64 (chunks of 64 columns)
         //   poly  (8 KiB):   2 bf16 input slots (A) + 2 output slots of bf16
-        //   axpy, axpy_o (8 KiB): 4 output slots of bf16 (axpy_o: O in the stored layout)
+        //   axpy_o (8 KiB):  4 output slots of bf16 (O in the stored layout)
+        // Gram and axpy take 64 columns per chunk: one slot wait, fence and TMA store per 32 x 64
+        // subtile halves that fixed cost per element, which bounds tiles with short K.
         const bool o_mode = P.mode == MODE_AXPY_O;
         const bool f32_out = final_mode;
+        const bool wide = P.mode == MODE_GRAM || P.mode == MODE_AXPY;
+        const int cw = wide ? 64 : 32;  // columns per chunk
         const int n_in = has_in ? 2 : 0;
         const int in_stride = 2048;
-        const int n_out = (f32_out || P.mode == MODE_POLY) ? 2 : 4;
-        const int out_stride = dbg_o ? 8192 : (f32_out ? 4096 : 2048);
+        const int n_out = (f32_out || wide || P.mode == MODE_POLY) ? 2 : 4;
+        const int out_stride = dbg_o ? 8192 : ((f32_out || wide) ? 4096 : 2048);
         uint8_t* out_base = wbase + n_in * in_stride;
         auto in_b16 = [&](int sl) { return wbase + sl * in_stride; };
         uint64_t* ibar = in_bar[lg];
@@ -397,20 +401,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int cb = pt.half_m ? (lg >> 1) * (pt.ncols >> 1) : 0;          // column offset in the tile
             const bool warp_rows = pt.rb < C.row_blocks && grow0 < C.m;
             const int climit = sym ? C.m : C.n;
-            const int nch = pt.half_m ? pt.ncols / 64 : pt.ncols / 32;
+            const int nch = (pt.half_m ? pt.ncols >> 1 : pt.ncols) / cw;
             const bool transposed = C.transposed != 0;
             const CUtensorMap* pmap = final_mode ? &P.p_maps[gm] : nullptr;
             // a chunk is live when this warp has rows, its columns exist, and (Gram/poly) its
             // 128-column block is not below the diagonal for this row block
             auto live = [&](int ch) {
-                const int cc0 = pt.c0 + cb + ch * 32;
+                const int cc0 = pt.c0 + cb + ch * cw;
                 if (!warp_rows || cc0 >= climit) return false;
                 if (sym && (cc0 >> 7) < pt.rb) return false;
                 return true;
             };
             auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0 (polynomial: the A tile)
                 const int slot = ch % n_in;
-                const int cc0 = pt.c0 + cb + ch * 32;
+                const int cc0 = pt.c0 + cb + ch * cw;
                 mbar_arrive_expect_tx(&ibar[slot], 2048u);
                 tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 in_pending_bits |= 1u << slot;
@@ -432,6 +436,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + static_cast<uint32_t>(acc * 256);
             bool failed = false;
             for (int ch = 0; ch < nch; ++ch) {
+                if (wide) {
+                    // Gram (A = s^2 acc) and axpy (X' = s acc): a 32 x 64 bf16 subtile per chunk
+                    uint32_t r0[32], r1[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(t_row + ch * 64, r0);
+                    tmem_ld_32x32b_x32(t_row + ch * 64 + 32, r1);
+                    tmem_ld_wait();
+                    if (ch == nch - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+                    }
+                    if (!live(ch)) continue;
+                    const int cc0 = pt.c0 + cb + ch * 64;
+                    const float f = P.mode == MODE_GRAM ? s * s : s;
+                    if (lane == 0) bulk_wait_group_read1();  // the slot's previous store has read it
+                    __syncwarp();
+                    uint8_t* out_slot = out_base + (groups & 1u) * out_stride;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t* q = u < 4 ? r0 + 8 * u : r1 + 8 * (u - 4);
+                        uint4 w;
+                        w.x = pack2(f * __uint_as_float(q[0]), f * __uint_as_float(q[1]));
+                        w.y = pack2(f * __uint_as_float(q[2]), f * __uint_as_float(q[3]));
+                        w.z = pack2(f * __uint_as_float(q[4]), f * __uint_as_float(q[5]));
+                        w.w = pack2(f * __uint_as_float(q[6]), f * __uint_as_float(q[7]));
+                        *reinterpret_cast<uint4*>(out_slot + sw128_unit(lane, u)) = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&P.tmOut[pt.ci], out_slot, cc0, grow0, pt.mat);
+                        bulk_commit_group();
+                        stores_issued = true;
+                    }
+                    ++groups;
+                    continue;
+                }
                 uint32_t raw_v[32];
                 __syncwarp();
                 tmem_ld_32x32b_x32(t_row + ch * 32, raw_v);
@@ -463,11 +505,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     }
                     if (failed) break;
                     // ---- the epilogue arithmetic, one oriented row (= lane) per thread
-                    if (P.mode == MODE_GRAM) {
-                        const float s2 = s * s;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= s2;
-                    } else if (P.mode == MODE_POLY) {
+                    if (P.mode == MODE_POLY) {
                         const uint8_t* xb = in_b16(slot);
                         const bool diag = cc0 == grow0;  // this 32 x 32 block holds diagonal entries
 #pragma unroll
