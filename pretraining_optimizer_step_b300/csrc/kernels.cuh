@@ -151,9 +151,8 @@ struct PairParams {
     CUtensorMap tmA[kMaxClasses];    // A side, K-major, box 64 (K) x 128 rows, 128B swizzle
     CUtensorMap tmB[kMaxClasses];    // B side: Gram/poly K-major box 64 x 64 (N = 128 tiles; N = 256 tiles
                                      // use tmA); axpy MN-major box 64 cols x 128 K
-    CUtensorMap tmIn[kMaxClasses];   // epilogue input (poly: A, axpy: X), bf16 box 32 x 32, 64B swizzle
-    CUtensorMap tmOut[kMaxClasses];  // epilogue output, bf16: gram A and axpy X' in boxes of 32 rows x 64 columns
-                                     // (128B swizzle), poly B' in 32 x 32 (64B swizzle)
+    CUtensorMap tmIn[kMaxClasses];   // epilogue input (poly: A), bf16 box 32 rows x 64 columns, 128B swizzle
+    CUtensorMap tmOut[kMaxClasses];  // epilogue output (gram: A, poly: B', axpy: X'), bf16 box 32 x 64, 128B swizzle
     CUtensorMap tmA64[kMaxClasses];  // A side of a half tile (M = 128): K-major box 64 (K) x 64 rows
     PairClass cls[kMaxClasses];
     int nclasses;

@@ -38,7 +38,7 @@ struct ClassPlan {
     // A-side K-major maps (box 64 x 128), B-side K-major maps (box 64 x 64), the MN-major X map
     // of the axpy B operand (box 64 x 128), and epilogue subtile maps (bf16 32 x 32)
     CUtensorMap tmXk[2], tmAk, tmBk;
-    CUtensorMap tmXk64[2], tmAk64, tmBk64, tmXmn128[2], epiX[2], epiA, epiB, epiX64[2], epiA64;
+    CUtensorMap tmXk64[2], tmAk64, tmBk64, tmXmn128[2], epiX64[2], epiA64, epiB64;
     int row_blocks = 0, col_tiles = 0;
     int col_pairs = 0, sym_pair_tiles = 0, axpy_pair_tiles = 0;
 };
@@ -328,9 +328,6 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
                 st = encode_map_ex(ctx->encode, &cp.tmXmn128[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 64, kPairBK,
                                    CU_TENSOR_MAP_SWIZZLE_128B);
             if (st == MUON_OK)
-                st = encode_map_ex(ctx->encode, &cp.epiX[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 32, 32,
-                                   CU_TENSOR_MAP_SWIZZLE_64B);
-            if (st == MUON_OK)
                 st = encode_map_ex(ctx->encode, &cp.epiX64[pp], bf, 2, cp.X[pp], cp.n, cp.m, G, 64, 32,
                                    CU_TENSOR_MAP_SWIZZLE_128B);
         }
@@ -339,11 +336,9 @@ muon_status build_plan(Context* ctx, const muon_shape* shapes, int n, Plan** out
         if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.tmBk64, bf, 2, cp.B, cp.m, cp.m, G, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st == MUON_OK)
-            st = encode_map_ex(ctx->encode, &cp.epiA, bf, 2, cp.A, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-        if (st == MUON_OK)
             st = encode_map_ex(ctx->encode, &cp.epiA64, bf, 2, cp.A, cp.m, cp.m, G, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st == MUON_OK)
-            st = encode_map_ex(ctx->encode, &cp.epiB, bf, 2, cp.B, cp.m, cp.m, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+            st = encode_map_ex(ctx->encode, &cp.epiB64, bf, 2, cp.B, cp.m, cp.m, G, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != MUON_OK) {
             free_plan(P);
             return st;
@@ -827,7 +822,6 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                         pp.tmA[k] = cp.tmXk[pin];
                         pp.tmB[k] = cp.tmXk64[pin];
                         pp.tmA64[k] = cp.tmXk64[pin];
-                        pp.tmIn[k] = cp.epiX[pin];
                         pp.tmOut[k] = cp.epiA64;
                     } else if (mode == MODE_POLY) {
                         C.tiles_per_mat = cp.sym_pair_tiles;
@@ -836,8 +830,8 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                         pp.tmA[k] = cp.tmAk;
                         pp.tmB[k] = cp.tmAk64;
                         pp.tmA64[k] = cp.tmAk64;
-                        pp.tmIn[k] = cp.epiA;
-                        pp.tmOut[k] = cp.epiB;
+                        pp.tmIn[k] = cp.epiA64;
+                        pp.tmOut[k] = cp.epiB64;
                     } else {
                         C.tiles_per_mat = cp.axpy_pair_tiles;
                         C.col_groups = cp.col_tiles;
@@ -845,7 +839,6 @@ static muon_status step_impl(float* const params[], const float* const grads[], 
                         pp.tmA[k] = cp.tmBk;
                         pp.tmB[k] = cp.tmXmn128[pin];
                         pp.tmA64[k] = cp.tmBk64;
-                        pp.tmIn[k] = cp.epiX[pin];
                         pp.tmOut[k] = cp.epiX64[pout];
                     }
                     tiles += C.tiles_per_mat * G;

@@ -46,14 +46,15 @@
 //               of both CTAs complete on the even CTA's mbarrier
 //   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues 8 MMAs
 //               (M 256, N 256/128, K 16) per stage and commits to both CTAs' barriers
-//   warps 2..5  epilogue (both CTAs): per warp 32 rows, in chunks of 32 columns.
-//               The polynomial's input (the A tile) arrives by TMA into a ring of
-//               swizzled shared slots, one chunk ahead; outputs leave by TMA store
-//               (reduce-add for the weights) from a ring of swizzled slots, and a
-//               slot is rewritten only once the store that last read it has read
-//               it (one bulk group per chunk).  Threads touch shared memory only
-//               with conflict-free 16-byte vectors (row access) or 4-byte/2-byte
-//               column access (transposes).
+//   warps 2..5  epilogue (both CTAs): per warp 32 rows, in chunks of 64 columns (Gram,
+//               polynomial, axpy: bf16) or 32 columns (the final launch's fp32 weight
+//               change, the bf16 O of the NorMuon step).  The polynomial's input (the A
+//               subtile) arrives by TMA one chunk ahead into a swizzled shared slot that
+//               then holds the chunk's output; outputs leave by TMA store (reduce-add
+//               for the weights) from swizzled slots, and a slot is rewritten only once
+//               the store that last read it has read it (one bulk group per chunk).
+//               Threads touch shared memory only with conflict-free 16-byte vectors
+//               (row access) or 4-byte/2-byte column access (transposes).
 // Every wait is bounded; on expiry the CTA latches STATUS_TIMEOUT, raises its
 // abort flag, lets its own copies land, and joins the final cluster barrier.
 // Launches use programmatic dependent launch: a launch's CTAs take the SMs the previous
@@ -363,23 +364,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const int lg = warp & 3;                       // TMEM lane group of this warp
         uint8_t* wbase = epi_ptr + lg * epi_warp_bytes;
         const bool has_in = P.mode == MODE_POLY;
-        // The warp's epilogue slots, by mode (an input slot holds chunk c when c % n_in == slot;
-        // loads run n_in - 1 chunks ahead; output slots alternate per committed store group, and
+        // The warp's epilogue slots, by mode (output slots alternate per committed store group, and
         // a slot is rewritten once the group that last read it -- n_out groups back -- has):
-        //   final (8 KiB):   2 output slots of the fp32 32x32 weight change -lr s O
+        //   gram, axpy (8 KiB): 2 output slots of a bf16 32 x 64 subtile
+        //   poly (8 KiB):    2 slots of a bf16 32 x 64 subtile, each first the input (the A subtile,
+        //                    loaded by TMA) and then, overwritten in place, the output B'; chunk c uses
+        //                    slot c % 2, and its slot is refilled with chunk c + 2 once chunk c's store
+        //                    has read it
+        //   final (8 KiB):   2 output slots of the fp32 32 x 32 weight change -lr s O
         //   final, debug copy of O (24 KiB): 2 output slot pairs {weight change, O} of 8 KiB
-        //   gram, axpy (8 KiB): 2 output slots of bf16 32 x 64 (chunks of 64 columns)
-        //   poly  (8 KiB):   2 bf16 input slots (A) + 2 output slots of bf16
-        //   axpy_o (8 KiB):  4 output slots of bf16 (O in the stored layout)
-        // Gram and axpy take 64 columns per chunk: one slot wait, fence and TMA store per 32 x 64
-        // subtile halves that fixed cost per element, which bounds tiles with short K.
-        const bool o_mode = P.mode == MODE_AXPY_O;
+        //   axpy_o (8 KiB):  4 output slots of bf16 32 x 32 (O in the stored layout)
+        // Gram, polynomial and axpy take 64 columns per chunk: one slot wait, fence and TMA store per
+        // 32 x 64 subtile halves that fixed cost per element, which bounds tiles with short K.
         const bool f32_out = final_mode;
-        const bool wide = P.mode == MODE_GRAM || P.mode == MODE_AXPY;
+        const bool wide = P.mode == MODE_GRAM || P.mode == MODE_AXPY || P.mode == MODE_POLY;
         const int cw = wide ? 64 : 32;  // columns per chunk
         const int n_in = has_in ? 2 : 0;
-        const int in_stride = 2048;
-        const int n_out = (f32_out || wide || P.mode == MODE_POLY) ? 2 : 4;
+        const int in_stride = 4096;
+        const int n_out = (f32_out || wide) ? 2 : 4;
         const int out_stride = dbg_o ? 8192 : ((f32_out || wide) ? 4096 : 2048);
         uint8_t* out_base = wbase + n_in * in_stride;
         auto in_b16 = [&](int sl) { return wbase + sl * in_stride; };
@@ -412,14 +414,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 if (sym && (cc0 >> 7) < pt.rb) return false;
                 return true;
             };
-            auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0 (polynomial: the A tile)
+            auto issue_in = [&](int ch) {  // lane 0 only; only when n_in > 0 (polynomial: the A subtile)
                 const int slot = ch % n_in;
                 const int cc0 = pt.c0 + cb + ch * cw;
-                mbar_arrive_expect_tx(&ibar[slot], 2048u);
+                mbar_arrive_expect_tx(&ibar[slot], 4096u);
                 tma_load_3d(in_b16(slot), &P.tmIn[pt.ci], &ibar[slot], cc0, grow0, pt.mat);
                 in_pending_bits |= 1u << slot;
             };
+            // polynomial: load chunk c + 2 into chunk c's slot, once every store has read its slot
+            auto refill = [&](int ch) {
+                if (has_in && lane == 0 && ch + n_in < nch && live(ch + n_in)) {
+                    bulk_wait_group_read0();
+                    issue_in(ch + n_in);
+                }
+            };
             if (has_in && lane == 0) {
+                bulk_wait_group_read0();  // the previous tile's last stores have read both slots
                 for (int ch = 0; ch < n_in && ch < nch; ++ch)
                     if (live(ch)) issue_in(ch);
             }
@@ -437,7 +447,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             bool failed = false;
             for (int ch = 0; ch < nch; ++ch) {
                 if (wide) {
-                    // Gram (A = s^2 acc) and axpy (X' = s acc): a 32 x 64 bf16 subtile per chunk
+                    // Gram (A = s^2 acc), axpy (X' = s acc) and polynomial (B' = c acc + b A + a I):
+                    // a 32 x 64 bf16 subtile per chunk
                     uint32_t r0[32], r1[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(t_row + ch * 64, r0);
@@ -448,20 +459,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                     }
-                    if (!live(ch)) continue;
+                    if (!live(ch)) {
+                        refill(ch);
+                        continue;
+                    }
                     const int cc0 = pt.c0 + cb + ch * 64;
-                    const float f = P.mode == MODE_GRAM ? s * s : s;
-                    if (lane == 0) bulk_wait_group_read1();  // the slot's previous store has read it
-                    __syncwarp();
-                    uint8_t* out_slot = out_base + (groups & 1u) * out_stride;
+                    float v[64];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        v[j] = __uint_as_float(r0[j]);
+                        v[32 + j] = __uint_as_float(r1[j]);
+                    }
+                    uint8_t* out_slot;
+                    if (has_in) {
+                        const int slot = ch & 1;
+                        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ibar[slot], (in_phase_bits >> slot) & 1u,
+                                                                                  &abort_flag, P.timeout_ns));
+                        if (!ok) {
+                            if (lane == 0) latch_status(P.status, STATUS_TIMEOUT);
+                            abort_flag = 1;
+                            failed = true;
+                            break;
+                        }
+                        in_phase_bits ^= 1u << slot;
+                        in_pending_bits &= ~(1u << slot);
+                        out_slot = in_b16(slot);
+                        // diagonal entries of this 32 x 64 subtile: column j = grow0 - cc0 + lane
+                        const int doff = grow0 - cc0;
+                        const int djl = (doff == 0 || doff == 32) ? doff + lane : -1;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(out_slot + sw128_unit(lane, u));
+                            const float a[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = 8 * u + e;
+                                v[j] = fmaf(P.cc, v[j], P.cb * a[e]) + (j == djl ? P.ca : 0.0f);
+                            }
+                        }
+                        __syncwarp();  // every lane has read the A subtile before B' overwrites it
+                    } else {
+                        const float f = P.mode == MODE_GRAM ? s * s : s;
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) v[j] *= f;
+                        if (lane == 0) bulk_wait_group_read1();  // the slot's previous store has read it
+                        __syncwarp();
+                        out_slot = out_base + (groups & 1u) * out_stride;
+                    }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const uint32_t* q = u < 4 ? r0 + 8 * u : r1 + 8 * (u - 4);
                         uint4 w;
-                        w.x = pack2(f * __uint_as_float(q[0]), f * __uint_as_float(q[1]));
-                        w.y = pack2(f * __uint_as_float(q[2]), f * __uint_as_float(q[3]));
-                        w.z = pack2(f * __uint_as_float(q[4]), f * __uint_as_float(q[5]));
-                        w.w = pack2(f * __uint_as_float(q[6]), f * __uint_as_float(q[7]));
+                        w.x = pack2(v[8 * u + 0], v[8 * u + 1]);
+                        w.y = pack2(v[8 * u + 2], v[8 * u + 3]);
+                        w.z = pack2(v[8 * u + 4], v[8 * u + 5]);
+                        w.w = pack2(v[8 * u + 6], v[8 * u + 7]);
                         *reinterpret_cast<uint4*>(out_slot + sw128_unit(lane, u)) = w;
                     }
                     fence_proxy_async_smem();
@@ -472,6 +524,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         stores_issued = true;
                     }
                     ++groups;
+                    refill(ch);
                     continue;
                 }
                 uint32_t raw_v[32];
@@ -484,45 +537,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                 }
-                const int slot = n_in > 0 ? ch % n_in : 0;
-                const bool lv = live(ch);
-                if (lv) {
+                // final and axpy_o: 32 x 32 subtiles (fp32 weight change, or bf16 O in the stored layout)
+                if (live(ch)) {
                     const int cc0 = pt.c0 + cb + ch * 32;
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw_v[j]);
-                    if (has_in) {
-                        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ibar[slot], (in_phase_bits >> slot) & 1u,
-                                                                                  &abort_flag, P.timeout_ns));
-                        if (!ok) {
-                            if (lane == 0) latch_status(P.status, STATUS_TIMEOUT);
-                            abort_flag = 1;
-                            failed = true;
-                        } else {
-                            in_phase_bits ^= 1u << slot;
-                            in_pending_bits &= ~(1u << slot);
-                        }
-                    }
-                    if (failed) break;
-                    // ---- the epilogue arithmetic, one oriented row (= lane) per thread
-                    if (P.mode == MODE_POLY) {
-                        const uint8_t* xb = in_b16(slot);
-                        const bool diag = cc0 == grow0;  // this 32 x 32 block holds diagonal entries
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(xb + sw64_unit(lane, u));
-                            const float a[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = 8 * u + e;
-                                v[j] = fmaf(P.cc, v[j], P.cb * a[e]) + ((diag && j == lane) ? P.ca : 0.0f);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= s;
-                    }
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw_v[j]) * s;
                     // the output slot about to be written must no longer be read by the store group
                     // that last used it, n_out groups back (the most recent n_out - 1 may still read)
                     if (lane == 0) {
@@ -558,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                     *reinterpret_cast<float*>(o_slot + sw128_elem(j, lane)) = v[j];
                             }
                         }
-                    } else if (o_mode && transposed) {
+                    } else if (transposed) {
                         // bf16 O subtile in the stored layout: stored rows are oriented columns j,
                         // stored columns are lanes (one 64-byte row per j, 2 bytes per lane)
 #pragma unroll
@@ -585,19 +605,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                 if (transposed) tma_store_2d(&P.dbg_maps[gm], out_slot + 4096, grow0, cc0);
                                 else tma_store_2d(&P.dbg_maps[gm], out_slot + 4096, cc0, grow0);
                             }
-                        } else if (o_mode) {
+                        } else {  // axpy_o
                             if (transposed) tma_store_2d(&P.o_maps[gm], out_slot, grow0, cc0);
                             else tma_store_2d(&P.o_maps[gm], out_slot, cc0, grow0);
-                        } else {
-                            tma_store_3d(&P.tmOut[pt.ci], out_slot, cc0, grow0, pt.mat);
                         }
                         bulk_commit_group();
                         stores_issued = true;
                     }
                     ++groups;  // every lane keeps the count (warp-uniform)
                 }
-                // refill this slot with the chunk n_in ahead
-                if (has_in && lane == 0 && ch + n_in < nch && live(ch + n_in)) issue_in(ch + n_in);
             }
             if (failed) break;
             if (++acc == 2) {
