@@ -223,9 +223,11 @@ MUON_API muon_status muon_get_step_info(muon_step_info* out);
  * oriented shape classes (matrices with equal (min side, max side,
  * transposed) share launches), kernel launches per step, workspace bytes,
  * algorithmic Newton-Schulz flops (3 m^2 n + m^3 per matrix and iteration),
- * executed tensor-core flops of the CTA-pair tiles (256 rows, or 128 for the
- * last row pair of a matrix with an odd number of 128-row blocks; diagonal and
- * ragged tiles included), algorithmic elementwise bytes (22 per element),
+ * executed tensor-core flops of the CTA-pair tiles (axpy: 256 rows, or 128 for
+ * the last row pair of a matrix with an odd number of 128-row blocks; Gram and
+ * polynomial: 256 x 256 tiles, diagonal ones included, except that with an odd
+ * block count each even diagonal block runs alone as a 128 x 128 tile; ragged
+ * tiles counted whole), algorithmic elementwise bytes (22 per element),
  * momentum CTAs, and pair tiles per Gram/polynomial launch and per axpy launch.
  * ns_steps is checked against the current context's table (16 rows without one).
  */

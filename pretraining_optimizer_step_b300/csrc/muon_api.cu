@@ -166,9 +166,12 @@ muon_status encode_f32_map(EncodeTiledFn enc, CUtensorMap* map, float* base, int
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// CTA-pair tiling: Gram/poly tiles per matrix (column pairs q, row pairs 0..q) and their
-// executed flops; axpy tiles per matrix (row pairs x 256-column tiles).  A row pair whose
-// second block does not exist (odd row_blocks, last pair) runs as M = 128 tiles.
+// CTA-pair tiling: Gram/poly tiles per matrix (column steps q, row pairs 0..q) and their
+// executed flops; axpy tiles per matrix (row pairs x 256-column tiles).  Gram/poly with an even
+// block count: 256 x 256 tiles, the diagonal ones included.  With an odd count: 256 x 256 tiles
+// off the diagonal (row pair rp x column blocks 2q-1, 2q) and each even diagonal block as an
+// M = 128, N = 128 tile.  An axpy row pair whose second block does not exist (odd row_blocks,
+// last pair) runs as M = 128 tiles.
 int pair_col_pairs(int row_blocks) { return (row_blocks + 1) / 2; }
 int pair_sym_tiles(int row_blocks) {
     const int Q = pair_col_pairs(row_blocks);
@@ -177,10 +180,9 @@ int pair_sym_tiles(int row_blocks) {
 double pair_rows(int row_blocks, int rp) { return 2 * rp + 1 < row_blocks ? 256.0 : 128.0; }
 double pair_sym_exec_flops(int row_blocks, int K) {
     double f = 0.0;
-    for (int q = 0; q < pair_col_pairs(row_blocks); ++q) {
-        const int ncols = (2 * q + 1 < row_blocks) ? 256 : 128;
-        for (int rp = 0; rp <= q; ++rp) f += 2.0 * pair_rows(row_blocks, rp) * ncols * K;
-    }
+    const bool odd = (row_blocks & 1) != 0;
+    for (int q = 0; q < pair_col_pairs(row_blocks); ++q)
+        for (int rp = 0; rp <= q; ++rp) f += (odd && rp == q ? 2.0 * 128 * 128 : 2.0 * 256 * 256) * K;
     return f;
 }
 double pair_axpy_exec_flops(int row_blocks, int n, int K) {

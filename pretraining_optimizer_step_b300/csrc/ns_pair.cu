@@ -20,9 +20,12 @@
 // operand and half of the N rows of the B operand in its shared memory, and
 // receives its 128 accumulator rows in its own TMEM.  Per SM this halves the B
 // operand traffic against a 128 x 256 single-CTA tile.
-//   Gram/poly: tile = row blocks (2 rp, 2 rp + 1) x column blocks (2 q, 2 q + 1),
-//              rp <= q; N = 128 when column block 2 q + 1 does not exist.  The
-//              lower block of a diagonal tile is computed but not stored.
+//   Gram/poly: with an even number of 128-row blocks, tile = row blocks (2 rp, 2 rp + 1)
+//              x column blocks (2 q, 2 q + 1), rp <= q; the lower block of a diagonal
+//              tile is computed but not stored.  With an odd number, tile = row blocks
+//              (2 rp, 2 rp + 1) x column blocks (2 q - 1, 2 q) for rp < q, and for rp = q
+//              the diagonal block 2 rp alone as an M = 128, N = 128 tile: every block
+//              on or above the diagonal is computed once and nothing below it.
 // Symmetric storage: A and B' are stored as their 128 x 128 blocks on and above
 // the diagonal (diagonal blocks in full); nothing below is written.  A GEMM that
 // reads A or B' as an operand takes a K panel that lies below the diagonal from
@@ -88,7 +91,7 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& P, int t,
     pt.mat = local / C.tiles_per_mat;
     const int lt = local - pt.mat * C.tiles_per_mat;
     if (sym) {
-        // column pair q has q + 1 tiles (row pairs 0..q)
+        // column step q has q + 1 tiles (row pairs rp = 0..q)
         int q = 0, base = 0;
         while (base + q + 1 <= lt) {
             base += q + 1;
@@ -96,16 +99,32 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& P, int t,
         }
         const int rp = lt - base;
         pt.rb0 = 2 * rp;
-        pt.c0 = 256 * q;
-        pt.ncols = (2 * q + 1 < C.row_blocks) ? 256 : 128;
+        if ((C.row_blocks & 1) == 0) {
+            // even block count: row blocks (2rp, 2rp+1) x column blocks (2q, 2q+1); the diagonal tile
+            // (rp = q) computes its lower block too
+            pt.c0 = 256 * q;
+            pt.ncols = 256;
+            pt.half_m = 0;
+        } else if (rp < q) {
+            // odd block count: row blocks (2rp, 2rp+1) x column blocks (2q-1, 2q), all on or above the
+            // diagonal
+            pt.c0 = 128 * (2 * q - 1);
+            pt.ncols = 256;
+            pt.half_m = 0;
+        } else {
+            // odd block count, rp = q: the diagonal block 2rp alone (M = 128, N = 128)
+            pt.c0 = 256 * rp;
+            pt.ncols = 128;
+            pt.half_m = 1;
+        }
     } else {
         const int rp = lt / C.col_groups;
         const int ct = lt - rp * C.col_groups;
         pt.rb0 = 2 * rp;
         pt.c0 = 256 * ct;
         pt.ncols = (C.n - pt.c0 > 128) ? 256 : 128;
+        pt.half_m = pt.rb0 + 1 >= C.row_blocks ? 1 : 0;
     }
-    pt.half_m = pt.rb0 + 1 >= C.row_blocks ? 1 : 0;
     pt.rb = pt.half_m ? pt.rb0 : pt.rb0 + rank;
     pt.row0 = pt.half_m ? pt.rb0 * 128 + 64 * rank : pt.rb * 128;
     return pt;
@@ -236,9 +255,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int a_first = pt.rb0;                 // the pair's first row block
             const int b_first = pt.c0 >> 7;             // the pair's first column block (poly)
             const uint32_t a_bytes = pt.half_m ? 16384u : 32768u;  // this CTA's A rows x 128 K
-            // a diagonal tile of a symmetric product with N = 256: each CTA's half of the B operand is
-            // its own A panel (same rows, K block and orientation), so only the A panels are loaded
-            const bool diag = sym && pt.ncols == 256 && b_first == a_first;
+            // a diagonal tile of a symmetric product (N = 256, or the M = 128 diagonal block): each CTA's
+            // half of the B operand is its own A panel (same rows, K block and orientation), so only the
+            // A panels are loaded
+            const bool diag = sym && b_first == a_first;
             const uint32_t total_bytes =
                 diag ? 2u * a_bytes : 2u * (a_bytes + static_cast<uint32_t>(half) * kPairBK * 2u);
             for (int kb = 0; kb < C.k_blocks; ++kb) {
@@ -308,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const bool a_symm = P.mode != MODE_GRAM;
             const int a_first = pt.rb0;           // the pair's first row block
             const int b_first = pt.c0 >> 7;
-            const bool diag = sym && pt.ncols == 256 && b_first == a_first;  // B halves = A panels
+            const bool diag = sym && b_first == a_first;  // B halves = A panels
             if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, &abort_flag, P.timeout_ns)) {
                 latch_status(P.status, STATUS_TIMEOUT);
                 abort_flag = 1;

@@ -68,27 +68,37 @@ def test_init_rejects_bad_configs_before_touching_the_device(L):
 def enumerate_pair_tiles(m, n):
     """Brute-force tile sets of the CTA-pair tiling (two 128-row blocks per tile).
 
-    Gram/polynomial: tile (rp, q) = row blocks 2rp, 2rp+1 x column blocks 2q, 2q+1
-    (those that exist), rp <= q.  Every 128 x 128 block on or above the diagonal
-    must be stored by exactly one tile (the lower block of a diagonal tile is not
-    stored).  Axpy: tile (rp, ct) = row blocks 2rp, 2rp+1 x 256 columns from
-    256 ct (128 when fewer than 129 remain).  A tile whose second row block does
-    not exist computes 128 rows (M = 128), every other 256.  Returns tile counts
-    and the executed flops per unit K (2 x rows x N per tile)."""
+    Gram/polynomial, rb = number of 128-row blocks: for column step q and row pair
+    rp <= q, with rb even the tile is row blocks 2rp, 2rp+1 x column blocks 2q,
+    2q+1 (the lower block of a diagonal tile is computed but not stored); with rb
+    odd it is row blocks 2rp, 2rp+1 x column blocks 2q-1, 2q for rp < q, and the
+    diagonal block 2rp alone (128 x 128) for rp = q.  Every 128 x 128 block on or
+    above the diagonal must be stored by exactly one tile.  Axpy: tile (rp, ct) =
+    row blocks 2rp, 2rp+1 x 256 columns from 256 ct (128 when fewer than 129
+    remain); a tile whose second row block does not exist computes 128 rows
+    (M = 128), every other 256.  Returns tile counts and the executed flops per
+    unit K (2 x rows x N per tile)."""
     rb = math.ceil(m / 128)
     sym, sym_f = [], 0
     stored = set()
     for q in range(math.ceil(rb / 2)):
-        cols = [c for c in (2 * q, 2 * q + 1) if c < rb]
         for rp in range(q + 1):
             sym.append((rp, q))
-            rows = 256 if 2 * rp + 1 < rb else 128
-            sym_f += 2 * rows * 128 * len(cols)
-            for i in (2 * rp, 2 * rp + 1):
+            if rb % 2 == 0:
+                rows, cols = (2 * rp, 2 * rp + 1), (2 * q, 2 * q + 1)
+            elif rp < q:
+                rows, cols = (2 * rp, 2 * rp + 1), (2 * q - 1, 2 * q)
+            else:
+                rows, cols = (2 * rp,), (2 * rp,)
+            assert all(i < rb for i in rows) and all(c < rb for c in cols)
+            sym_f += 2 * 128 * len(rows) * 128 * len(cols)
+            for i in rows:
                 for c in cols:
-                    if i < rb and i <= c:
+                    if i <= c:
                         assert (i, c) not in stored
                         stored.add((i, c))
+                    else:
+                        assert rb % 2 == 0 and rp == q  # only the even-count diagonal tile computes a lower block
     assert stored == {(i, j) for i in range(rb) for j in range(i, rb)}
     axpy, axpy_f = 0, 0
     for rp in range(math.ceil(rb / 2)):

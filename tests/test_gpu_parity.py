@@ -68,7 +68,7 @@ def test_d2_short_iterations(ns_steps):
 
 
 RAGGED = [(136, 200), (200, 136), (8, 8), (8, 1024), (1024, 8), (264, 264), (128, 384), (384, 128),
-          (520, 64), (392, 1032), (1032, 392)]
+          (520, 64), (392, 1032), (1032, 392), (520, 1040), (1040, 520)]
 
 
 def small_side_tol(shape):
