@@ -651,9 +651,17 @@ def run_sweep(args) -> int:
         ns_ms = sum(kt[k][0] for k in ("gram", "poly", "axpy", "axpy_update")) / nsteps
         mom_ms = kt["momentum_norm"][0] / nsteps
         ms = statistics.median(times)
+        # ideal NS bytes per matrix and iteration: X read twice and written once (bf16, 6mn), A written
+        # and read twice, B' written and read (bf16, 5m^2); below the ridge this is the bound
+        ns_bytes = workloads.HYPER["ns_steps"] * count * (6.0 * mm * nn + 5.0 * mm * mm)
+        intensity = info["ns_alg_flops"] / ns_bytes
+        ridge = peak_sus * 1e12 / (peak_bw * 1e9)
         rows.append({"workload": name, "shape": [r, c], "matrices": count, "steps": nsteps, "ms_per_step": ms,
                      "ns_tflops": info["ns_alg_flops"] / (ns_ms * 1e-3) / 1e12,
                      "ns_frac_of_sustained_bf16": info["ns_alg_flops"] / (ns_ms * 1e-3) / 1e12 / peak_sus,
+                     "ns_flop_per_byte": intensity, "ns_bound": "tensor" if intensity >= ridge else "hbm",
+                     "ns_alg_gbs": ns_bytes / (ns_ms * 1e-3) / 1e9,
+                     "ns_frac_of_hbm": ns_bytes / (ns_ms * 1e-3) / 1e9 / peak_bw,
                      "executed_over_alg_flops": q["ns_executed_flops"] / q["ns_alg_flops"],
                      "momentum_gbs": 14.0 * count * r * c / (mom_ms * 1e-3) / 1e9,
                      "momentum_frac_of_hbm": 14.0 * count * r * c / (mom_ms * 1e-3) / 1e9 / peak_bw,
