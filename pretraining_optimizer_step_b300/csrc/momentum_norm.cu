@@ -63,6 +63,21 @@ __global__ void __launch_bounds__(kMomThreads)
     const float omb = 1.0f - beta;
 
     float ss = 0.0f;
+    // all four rows' loads are issued before the first store (the compiler cannot prove that g and
+    // the momentum buffer do not alias, so it would not move a load above an earlier store)
+    float4 gv[4], mv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int row = r0 + rr + 16 * k;
+        const int col = c0 + 4 * cq;
+        gv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        mv[k] = gv[k];
+        if (row < M.rows && col < M.cols) {
+            const size_t off = static_cast<size_t>(row) * M.cols + col;
+            gv[k] = __ldcs(reinterpret_cast<const float4*>(M.g + off));
+            mv[k] = __ldcs(reinterpret_cast<const float4*>(M.mom + off));
+        }
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int row = r0 + rr + 16 * k;
@@ -70,8 +85,8 @@ __global__ void __launch_bounds__(kMomThreads)
         float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row < M.rows && col < M.cols) {
             const size_t off = static_cast<size_t>(row) * M.cols + col;
-            const float4 g4 = __ldcs(reinterpret_cast<const float4*>(M.g + off));
-            const float4 m4 = __ldcs(reinterpret_cast<const float4*>(M.mom + off));
+            const float4 g4 = gv[k];
+            const float4 m4 = mv[k];
             float4 n4;
             if (P.mode == 1) {
                 n4.x = fmaf(beta, m4.x, omb * g4.x);
