@@ -39,6 +39,11 @@
  *    orders its work only after earlier work on its own `stream`.  Steps issued
  *    on different streams must therefore be ordered by the caller (an event, or
  *    one stream for all of them); steps that overlap on the GPU race.
+ *  - The library's kernels let the next kernel on the stream begin launching
+ *    early (programmatic dependent launch).  Ordinary launches are unaffected;
+ *    a caller's kernel launched with programmatic stream serialization must, as
+ *    CUDA requires of any such kernel, execute griddepcontrol.wait before it
+ *    reads what the step wrote.
  */
 #ifndef MUON_H
 #define MUON_H
