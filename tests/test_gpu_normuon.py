@@ -95,6 +95,16 @@ def test_d12_sampled():
     step_and_check(p, g, m, zeros_state(shapes), check_idx=[0, 4, 5, 70, 71])
 
 
+@pytest.mark.slow
+def test_d26_sampled():
+    # the configuration the benchmark's NorMuon leg times (the full d26 stack, a zero state);
+    # the oracle checks the first and last layers' square, tall and wide matrices
+    p, g, m, shapes = workloads.make_stack("d26", "cuda")
+    n = len(p)
+    assert shapes[4] == (6656, 1664) and shapes[n - 1] == (1664, 6656)
+    step_and_check(p, g, m, zeros_state(shapes), check_idx=[0, 4, 5, n - 6, n - 2, n - 1])
+
+
 def test_zero_gradient_leaves_weights_and_decays_state():
     shapes = [(64, 64), (256, 64), (64, 256)]
     p = [torch.randn(s, device="cuda") for s in shapes]
