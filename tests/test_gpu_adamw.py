@@ -81,8 +81,10 @@ def test_zero_weight_decay_and_large_eps():
     run_steps([4096, 33], steps=2, hp=dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-3, weight_decay=0.0), seed=5)
 
 
-def test_d12_adamw_set_sampled():
-    p, g, m, v, shapes = workloads.make_adamw_set("d12", "cuda")
+@pytest.mark.parametrize("name", ["d12", "d26"])
+def test_adamw_set_sampled(name):
+    # d26's set is the one the benchmark's AdamW leg times
+    p, g, m, v, shapes = workloads.make_adamw_set(name, "cuda")
     host = [[t.cpu().numpy().reshape(-1).copy() for t in (p[i], g[i], m[i], v[i])] for i in range(len(p))]
     mu.muon_adamw_step(p, g, m, v, step=7, **HP)
     torch.cuda.synchronize()
