@@ -237,17 +237,6 @@ def test_d26_full_stack_sampled():
     run_and_check(p, g, m, check_idx=[0, 4, 5, n - 6, n - 2, n - 1])
 
 
-@pytest.mark.slow
-def test_d20_full_stack_sampled():
-    # the full d20 stack (m = 1280: an even count of 128-row blocks, so the Gram/polynomial tiles with
-    # a computed lower diagonal block) in the configuration the benchmark times; the oracle checks
-    # the first and last layers' six matrices
-    p, g, m, shapes = workloads.make_stack("d20", "cuda")
-    n = len(p)
-    assert shapes[4] == (5120, 1280) and shapes[n - 1] == (1280, 5120)
-    run_and_check(p, g, m, check_idx=[0, 4, 5, n - 6, n - 2, n - 1])
-
-
 def test_many_classes_and_matrices_span_several_launches():
     # 10 distinct oriented shapes (two launch groups of at most 8 classes per GEMM mode) and
     # 200 matrices (two momentum launches of at most 192 matrices)
